@@ -1,0 +1,305 @@
+"""Plain float64 CPU oracle for context-parallel attention (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may use this module. It shares no code with the CUDA library.
+
+Sources. The diffusers documentation pages on context parallelism:
+  [CP]  "Paralelismo de contexto" / "コンテキスト並列" (optimization/context_parallelism),
+        sections Ring Attention, Ulysses Attention, Unified Attention,
+        Ring Anything Attention, and the variant/requirements table at the top;
+  [API] "Paralelismo" (api/parallel), ContextParallelConfig parameters
+        ring_degree, ulysses_degree, convert_to_fp32, ring_anything, mesh.
+The pages never write out the attention or merge formulas; where they are
+silent the plainest reading is taken and named below (readings R1..R9).
+
+Layouts: q, k, v, out are [B, S, H, D] (D fastest); lse is [B, H, S], natural
+log (R1, R2). Inputs may be any float dtype; they are upcast to float64 first,
+so the oracle sees exactly the values the GPU sees.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+class NotDivisibleError(ValueError):
+    """A length is not divisible by a degree that the variant requires to divide it."""
+
+
+class UnsupportedComboError(ValueError):
+    """A flag combination the requirements table rules out."""
+
+
+def _f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # a torch tensor: go through float32 (exact for bf16/f32)
+        x = x.detach().to("cpu").float().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Block attention: the per-step computation of a ring lap.
+# [API] ring_degree: "each device computes attention between its local Q and
+# the KV blocks passed around the ring"; [API] convert_to_fp32: the step
+# returns an output and an LSE (kept in fp32 for the merge).
+# Reading R1: LSE is the natural-log log-sum-exp of the *scaled* logits.
+# Reading R3: non-causal, no mask, no dropout ([CP] Ring Anything note:
+# inference only, attn_mask must be None).
+# ---------------------------------------------------------------------------
+def attention(q, k, v, scale: float, row_chunk: int = 1024):
+    """Softmax attention of q against one K/V block, returning (out, lse).
+
+    For each batch b, head h and query row i:
+        s_ij   = scale * sum_d q[b,i,h,d] * k[b,j,h,d]
+        m_i    = max_j s_ij
+        w_ij   = exp(s_ij - m_i),   l_i = sum_j w_ij
+        out    = sum_j w_ij v[b,j,h,:] / l_i
+        lse    = m_i + ln(l_i)
+    An empty block (Skv = 0) gives out = 0 and lse = -inf (reading R6), the
+    identity element of ``lse_merge``.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    assert k.shape == (B, Skv, H, D) and v.shape == (B, Skv, H, D)
+    out = np.zeros((B, Sq, H, D), dtype=np.float64)
+    lse = np.full((B, H, Sq), NEG_INF, dtype=np.float64)
+    if Skv == 0 or Sq == 0:
+        return out, lse
+    for b in range(B):
+        for h in range(H):
+            kt = k[b, :, h, :].T
+            vb = v[b, :, h, :]
+            for i0 in range(0, Sq, row_chunk):
+                i1 = min(Sq, i0 + row_chunk)
+                s = scale * (q[b, i0:i1, h, :] @ kt)
+                m = s.max(axis=1, keepdims=True)
+                w = np.exp(s - m)
+                l = w.sum(axis=1, keepdims=True)
+                out[b, i0:i1, h, :] = (w @ vb) / l
+                lse[b, h, i0:i1] = (m + np.log(l))[:, 0]
+    return out, lse
+
+
+def attention_rows(q, k, v, scale: float, rows):
+    """``attention`` for selected query rows only (rows are independent)."""
+    q = _f64(q)
+    return attention(q[:, np.asarray(rows)], k, v, scale)
+
+
+# ---------------------------------------------------------------------------
+# LSE merge of two (out, lse) partials.
+# [API] convert_to_fp32 ("output and LSE in float32 for the numerical
+# stability of ring attention") implies each step yields (out, lse) and the
+# steps are combined through the LSE. Reading R4: the merge is the exact
+# recombination of two softmax-normalised partials over disjoint key sets:
+#     lse = m + ln(e^{lse_a - m} + e^{lse_b - m}),  m = max(lse_a, lse_b)
+#     out = e^{lse_a - lse} out_a + e^{lse_b - lse} out_b
+# with both-empty rows (m = -inf) giving (0, -inf).
+# ---------------------------------------------------------------------------
+def lse_merge(out_a, lse_a, out_b, lse_b):
+    out_a, lse_a, out_b, lse_b = _f64(out_a), _f64(lse_a), _f64(out_b), _f64(lse_b)
+    m = np.maximum(lse_a, lse_b)
+    empty = np.isneginf(m)
+    m_safe = np.where(empty, 0.0, m)
+    with np.errstate(invalid="ignore"):
+        tot = np.exp(lse_a - m_safe) + np.exp(lse_b - m_safe)
+        lse = np.where(empty, NEG_INF, m_safe + np.log(np.where(empty, 1.0, tot)))
+        lse_safe = np.where(empty, 0.0, lse)
+        wa = np.where(empty, 0.0, np.exp(lse_a - lse_safe))
+        wb = np.where(empty, 0.0, np.exp(lse_b - lse_safe))
+    # weights are per (b, h, s); out rows are (b, s, h, :)
+    wa_o = np.transpose(wa, (0, 2, 1))[..., None]
+    wb_o = np.transpose(wb, (0, 2, 1))[..., None]
+    out = wa_o * out_a + wb_o * out_b
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# Shard table ([CP] requirements table; Ring Anything section).
+# Plain ring needs S % ring_degree == 0. Ring Anything pads each rank's K/V
+# to the longest local length and slices each block back to its true length;
+# the pages do not say how S is split. Reading R5: balanced split, the first
+# S mod N shards get ceil(S/N) tokens and the rest floor(S/N).
+# ---------------------------------------------------------------------------
+def ring_shard_table(S: int, n: int, uneven_ok: bool):
+    """Contiguous token ranges [(offset, length)] of the n ring ranks."""
+    if n < 1 or S < 0:
+        raise ValueError("ring degree must be >= 1 and S >= 0")
+    base, extra = divmod(S, n)
+    if extra and not uneven_ok:
+        raise NotDivisibleError(f"sequence length {S} is not divisible by ring_degree {n}")
+    table, off = [], 0
+    for r in range(n):
+        ln = base + (1 if r < extra else 0)
+        table.append((off, ln))
+        off += ln
+    return table
+
+
+# ---------------------------------------------------------------------------
+# Ring lap ([CP] Ring Attention: K/V blocks pass around a ring; each GPU
+# attends to the block it holds, then passes it on; after a full lap every
+# GPU has seen every token's K/V). Reading R7: at step t rank r holds the
+# block of rank (r - t) mod N (it receives from its predecessor, own block
+# first). The accumulator starts as the t = 0 partial.
+# ---------------------------------------------------------------------------
+def _ring_lap_rows(q_r, k, v, scale, table, r):
+    n = len(table)
+    acc = None
+    for t in range(n):
+        j = (r - t) % n
+        off, ln = table[j]
+        part = attention(q_r, k[:, off:off + ln], v[:, off:off + ln], scale)
+        acc = part if acc is None else lse_merge(acc[0], acc[1], part[0], part[1])
+    return acc
+
+
+def ring_attention(q, k, v, scale: float, ring_degree: int, uneven_ok: bool = False):
+    """Simulated ring lap over ``ring_degree`` ranks; returns global (out, lse)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, S, H, D = q.shape
+    table = ring_shard_table(S, ring_degree, uneven_ok)
+    out = np.zeros((B, S, H, D))
+    lse = np.full((B, H, S), NEG_INF)
+    for r, (off, ln) in enumerate(table):
+        o_r, l_r = _ring_lap_rows(q[:, off:off + ln], k, v, scale, table, r)
+        out[:, off:off + ln] = o_r
+        lse[:, :, off:off + ln] = l_r
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# Ulysses regroups ([CP] Ulysses Attention: the first all-to-all regroups so
+# that each GPU holds every token for a subset of heads; the second regroups
+# the results back by token). Reading R8: contiguous head groups
+# g*H/U .. (g+1)*H/U - 1; tokens concatenated in rank order.
+#   seq2head: out_g[b, u*S/U + s, h, d] = in_u[b, s, g*H/U + h, d]
+#   head2seq: out_u[b, s, g*H/U + h, d] = in_g[b, u*S/U + s, h, d]
+# Written as explicit index loops (slabs of one head), not as a reshape, so
+# that a reshape/transpose formulation can check it independently.
+# ---------------------------------------------------------------------------
+def seq2head(x_shards):
+    """[U][B, S/U, H, D] (sequence-sharded) -> [U][B, S, H/U, D] (head-sharded)."""
+    x = np.asarray(x_shards)
+    U, B, Sl, H, D = x.shape
+    if H % U:
+        raise NotDivisibleError(f"heads {H} not divisible by ulysses_degree {U}")
+    Hg = H // U
+    out = np.empty((U, B, Sl * U, Hg, D), dtype=x.dtype)
+    for g in range(U):
+        for u in range(U):
+            for h in range(Hg):
+                out[g, :, u * Sl:(u + 1) * Sl, h, :] = x[u, :, :, g * Hg + h, :]
+    return out
+
+
+def head2seq(x_groups):
+    """[U][B, S, H/U, D] (head-sharded) -> [U][B, S/U, H, D] (sequence-sharded)."""
+    x = np.asarray(x_groups)
+    U, B, S, Hg, D = x.shape
+    if S % U:
+        raise NotDivisibleError(f"sequence {S} not divisible by ulysses_degree {U}")
+    Sl = S // U
+    out = np.empty((U, B, Sl, Hg * U, D), dtype=x.dtype)
+    for u in range(U):
+        for g in range(U):
+            for h in range(Hg):
+                out[u, :, :, g * Hg + h, :] = x[g, :, u * Sl:(u + 1) * Sl, h, :]
+    return out
+
+
+def head2seq_lse(lse_groups):
+    """[U][B, H/U, S] per-group LSE -> [B, H, S]: lse[b, g*H/U + h, s] = lse_g[b, h, s]."""
+    x = np.asarray(lse_groups)
+    U, B, Hg, S = x.shape
+    out = np.empty((B, Hg * U, S), dtype=x.dtype)
+    for g in range(U):
+        for h in range(Hg):
+            out[:, g * Hg + h, :] = x[g, :, h, :]
+    return out
+
+
+def _split_seq(x, n):
+    B, S = x.shape[:2]
+    Sl = S // n
+    return np.stack([x[:, u * Sl:(u + 1) * Sl] for u in range(n)])
+
+
+def ulysses_attention(q, k, v, scale: float, ulysses_degree: int):
+    """All-to-all, attention over all tokens of a head group, inverse all-to-all."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, S, H, D = q.shape
+    U = ulysses_degree
+    if S % U or H % U:
+        raise NotDivisibleError(f"S={S} and H={H} must be divisible by ulysses_degree {U}")
+    qh, kh, vh = (seq2head(_split_seq(t, U)) for t in (q, k, v))
+    outs, lses = [], []
+    for g in range(U):
+        o, l = attention(qh[g], kh[g], vh[g], scale)
+        outs.append(o)
+        lses.append(l)
+    out = np.concatenate(list(head2seq(np.stack(outs))), axis=1)
+    lse = head2seq_lse(np.stack(lses))
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# Unified sequence parallelism ([CP] Unified Attention: an all-to-all
+# redistributes heads and tokens, ring attention runs on the result, then the
+# all-to-all is reversed; the devices form a 2D ulysses x ring grid with
+# orthogonal groups). Reading R9: mesh dims ("ring", "ulysses") as in [API]
+# mesh; device (r, u) holds token chunk r*U + u of S/(R*U) tokens; Ulysses
+# group r is ring row r, which after its regroup holds tokens
+# [r*S/R, (r+1)*S/R) for head group u.
+# ---------------------------------------------------------------------------
+def unified_attention(q, k, v, scale: float, ring_degree: int, ulysses_degree: int):
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, S, H, D = q.shape
+    R, U = ring_degree, ulysses_degree
+    if S % (R * U) or H % U:
+        raise NotDivisibleError(f"S={S} must be divisible by {R * U} and H={H} by {U}")
+    Sr = S // R
+    # per ring row r: seq2head inside the Ulysses group -> [U][B, S/R, H/U, D]
+    rows = []
+    for r in range(R):
+        blk = [t[:, r * Sr:(r + 1) * Sr] for t in (q, k, v)]
+        rows.append([seq2head(_split_seq(t, U)) for t in blk])
+    out = np.zeros((B, S, H, D))
+    lse = np.zeros((B, H, S))
+    for r in range(R):
+        outs, lses = [], []
+        for g in range(U):
+            acc = None
+            for t in range(R):
+                j = (r - t) % R
+                part = attention(rows[r][0][g], rows[j][1][g], rows[j][2][g], scale)
+                acc = part if acc is None else lse_merge(acc[0], acc[1], part[0], part[1])
+            outs.append(acc[0])
+            lses.append(acc[1])
+        out[:, r * Sr:(r + 1) * Sr] = np.concatenate(list(head2seq(np.stack(outs))), axis=1)
+        lse[:, :, r * Sr:(r + 1) * Sr] = head2seq_lse(np.stack(lses))
+    return out, lse
+
+
+def cp_attention(q, k, v, scale: float, ring_degree: int = 1, ulysses_degree: int = 1,
+                 uneven_ok: bool = False):
+    """Dispatch on the ContextParallelConfig degrees ([CP] variants table).
+
+    Ring (ring_degree > 1), Ulysses (ulysses_degree > 1), Unified (both > 1),
+    Ring Anything (ring_degree > 1 with uneven_ok; ulysses_degree must be 1).
+    """
+    q = _f64(q)
+    B, S, H, D = q.shape
+    R, U = ring_degree, ulysses_degree
+    if R < 1 or U < 1:
+        raise ValueError("degrees must be >= 1")
+    if uneven_ok and (U != 1 or R < 2):
+        raise UnsupportedComboError("Ring Anything needs ring_degree > 1 and ulysses_degree == 1")
+    if U > H:
+        raise ValueError(f"ulysses_degree {U} exceeds the number of heads {H}")
+    if U == 1:
+        return ring_attention(q, k, v, scale, R, uneven_ok)
+    if R == 1:
+        return ulysses_attention(q, k, v, scale, U)
+    return unified_attention(q, k, v, scale, R, U)

@@ -1,0 +1,418 @@
+"""Pins of the float64 oracle against things other than itself (CPU only).
+
+Each pin is one of: brute force with a different formulation, a closed form,
+an invariant of softmax attention, a library routine (scipy/numpy) on a
+special case, or a value fixed by the pages (tests/golden). The last group
+plants mistakes into copies of the oracle and checks that some pin fails.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+from oracle import cp_oracle as co
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rnd(shape, seed, scale=1.0):
+    return scale * np.random.default_rng(seed).standard_normal(shape)
+
+
+# ----------------------------------------------------------------------------
+# attention
+# ----------------------------------------------------------------------------
+def brute_attention(q, k, v, scale):
+    """Scalar loops, no max shift: p_j = e^{s_j} / sum_k e^{s_k}, lse = ln sum e^{s}."""
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    out = np.zeros((B, Sq, H, D))
+    lse = np.zeros((B, H, Sq))
+    for b in range(B):
+        for h in range(H):
+            for i in range(Sq):
+                s = [scale * math.fsum(q[b, i, h, d] * k[b, j, h, d] for d in range(D))
+                     for j in range(Skv)]
+                e = [math.exp(x) for x in s]
+                z = math.fsum(e)
+                lse[b, h, i] = math.log(z)
+                for d in range(D):
+                    out[b, i, h, d] = math.fsum(e[j] * v[b, j, h, d] for j in range(Skv)) / z
+    return out, lse
+
+
+@pytest.mark.parametrize("B,Sq,Skv,H,D,seed", [(1, 3, 5, 1, 2, 0), (2, 4, 7, 2, 3, 1),
+                                                 (1, 8, 1, 2, 4, 2), (2, 1, 8, 3, 4, 3)])
+def test_attention_matches_brute_force(B, Sq, Skv, H, D, seed):
+    q, k, v = rnd((B, Sq, H, D), seed), rnd((B, Skv, H, D), seed + 10), rnd((B, Skv, H, D), seed + 20)
+    scale = 0.7
+    o, l = oracle.attention(q, k, v, scale)
+    ob, lb = brute_attention(q, k, v, scale)
+    assert np.max(np.abs(o - ob)) <= 1e-13
+    assert np.max(np.abs(l - lb)) <= 1e-13
+
+
+def test_attention_matches_scipy_softmax_logsumexp():
+    q, k, v = rnd((2, 9, 3, 16), 4), rnd((2, 33, 3, 16), 5), rnd((2, 33, 3, 16), 6)
+    scale = 0.25
+    o, l = oracle.attention(q, k, v, scale)
+    for b in range(2):
+        for h in range(3):
+            s = scale * np.einsum("id,jd->ij", q[b, :, h], k[b, :, h])
+            np.testing.assert_allclose(l[b, h], scipy.special.logsumexp(s, axis=1), rtol=0, atol=1e-12)
+            p = scipy.special.softmax(s, axis=1)
+            np.testing.assert_allclose(o[b, :, h], p @ v[b, :, h], rtol=0, atol=1e-12)
+
+
+def test_rows_sum_to_one():
+    q, k = rnd((1, 17, 2, 8), 7, 3.0), rnd((1, 40, 2, 8), 8, 3.0)
+    v = np.ones((1, 40, 2, 8))
+    o, _ = oracle.attention(q, k, v, 0.5)
+    assert np.max(np.abs(o - 1.0)) <= 1e-14
+
+
+def test_constant_keys_give_mean_of_v():
+    B, Sq, Skv, H, D = 1, 5, 11, 2, 4
+    q, v = rnd((B, Sq, H, D), 9), rnd((B, Skv, H, D), 10)
+    c = rnd((H, D), 11)
+    k = np.broadcast_to(c[None, None], (B, Skv, H, D)).copy()
+    scale = 0.6
+    o, l = oracle.attention(q, k, v, scale)
+    mean_v = v.mean(axis=1, keepdims=True)
+    np.testing.assert_allclose(o, np.broadcast_to(mean_v, o.shape), rtol=0, atol=1e-14)
+    expect_lse = scale * np.einsum("bihd,hd->bhi", q, c) + math.log(Skv)
+    np.testing.assert_allclose(l, expect_lse, rtol=0, atol=1e-13)
+
+
+def test_zero_query_gives_mean_and_log_count():
+    q = np.zeros((1, 3, 2, 4))
+    k, v = rnd((1, 13, 2, 4), 12), rnd((1, 13, 2, 4), 13)
+    o, l = oracle.attention(q, k, v, 1.0)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(axis=1, keepdims=True), o.shape), atol=1e-14, rtol=0)
+    np.testing.assert_allclose(l, math.log(13), atol=1e-14, rtol=0)
+
+
+def test_single_key():
+    q, k, v = rnd((2, 6, 2, 4), 14), rnd((2, 1, 2, 4), 15), rnd((2, 1, 2, 4), 16)
+    o, l = oracle.attention(q, k, v, 0.3)
+    np.testing.assert_array_equal(o, np.broadcast_to(v, o.shape))
+    np.testing.assert_allclose(l, 0.3 * np.einsum("bihd,bhd->bhi", q, k[:, 0]), atol=1e-14, rtol=0)
+
+
+def test_two_keys_closed_form():
+    q, k, v = rnd((1, 4, 1, 3), 17), rnd((1, 2, 1, 3), 18), rnd((1, 2, 1, 3), 19)
+    scale = 0.9
+    o, l = oracle.attention(q, k, v, scale)
+    s0 = scale * q[0, :, 0] @ k[0, 0, 0]
+    s1 = scale * q[0, :, 0] @ k[0, 1, 0]
+    sig = 1.0 / (1.0 + np.exp(-(s0 - s1)))  # logistic weight of key 0
+    expect = sig[:, None] * v[0, 0, 0] + (1 - sig)[:, None] * v[0, 1, 0]
+    np.testing.assert_allclose(o[0, :, 0], expect, atol=1e-14, rtol=0)
+    np.testing.assert_allclose(l[0, 0], np.logaddexp(s0, s1), atol=1e-14, rtol=0)
+
+
+def test_key_shift_invariance():
+    q, k, v = rnd((1, 7, 2, 5), 20), rnd((1, 9, 2, 5), 21), rnd((1, 9, 2, 5), 22)
+    delta = rnd((2, 5), 23)
+    scale = 0.4
+    o1, l1 = oracle.attention(q, k, v, scale)
+    o2, l2 = oracle.attention(q, k + delta[None, None], v, scale)
+    np.testing.assert_allclose(o2, o1, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(l2 - l1, scale * np.einsum("bihd,hd->bhi", q, delta), atol=1e-12, rtol=0)
+
+
+def test_joint_kv_permutation_invariance():
+    q, k, v = rnd((2, 5, 3, 4), 24), rnd((2, 12, 3, 4), 25), rnd((2, 12, 3, 4), 26)
+    perm = np.random.default_rng(27).permutation(12)
+    o1, l1 = oracle.attention(q, k, v, 0.8)
+    o2, l2 = oracle.attention(q, k[:, perm], v[:, perm], 0.8)
+    np.testing.assert_allclose(o2, o1, atol=1e-14, rtol=0)
+    np.testing.assert_allclose(l2, l1, atol=1e-13, rtol=0)
+
+
+def test_dominant_key():
+    D = 4
+    q = np.zeros((1, 1, 1, D)); q[0, 0, 0, 0] = 10.0
+    k = rnd((1, 6, 1, D), 28, 0.1)
+    k[0, 3, 0, 0] = 8.0          # logit 80 vs |others| < ~3: gap > 50
+    v = rnd((1, 6, 1, D), 29)
+    o, l = oracle.attention(q, k, v, 1.0)
+    np.testing.assert_allclose(o[0, 0, 0], v[0, 3, 0], atol=1e-20 + 1e-14, rtol=0)
+    assert abs(l[0, 0, 0] - 80.0) < 1e-20 + 1e-12
+
+
+def test_empty_block_is_merge_identity():
+    q = rnd((1, 3, 2, 4), 30)
+    o, l = oracle.attention(q, np.zeros((1, 0, 2, 4)), np.zeros((1, 0, 2, 4)), 1.0)
+    assert np.all(o == 0) and np.all(np.isneginf(l))
+
+
+def test_heads_and_batches_independent():
+    q, k, v = rnd((2, 4, 3, 4), 31), rnd((2, 6, 3, 4), 32), rnd((2, 6, 3, 4), 33)
+    o, l = oracle.attention(q, k, v, 0.5)
+    for b in range(2):
+        for h in range(3):
+            ob, lb = oracle.attention(q[b:b + 1, :, h:h + 1], k[b:b + 1, :, h:h + 1], v[b:b + 1, :, h:h + 1], 0.5)
+            np.testing.assert_array_equal(o[b:b + 1, :, h:h + 1], ob)
+            np.testing.assert_array_equal(l[b:b + 1, h:h + 1], lb)
+
+
+def test_row_sampling_matches_full():
+    q, k, v = rnd((1, 20, 2, 4), 34), rnd((1, 15, 2, 4), 35), rnd((1, 15, 2, 4), 36)
+    o, l = oracle.attention(q, k, v, 0.5)
+    rows = [0, 7, 19]
+    os_, ls_ = oracle.attention_rows(q, k, v, 0.5, rows)
+    np.testing.assert_array_equal(os_, o[:, rows])
+    np.testing.assert_array_equal(ls_, l[:, :, rows])
+
+
+# ----------------------------------------------------------------------------
+# merge
+# ----------------------------------------------------------------------------
+def merged_over_partition(q, k, v, scale, cuts):
+    acc = None
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        part = oracle.attention(q, k[:, a:b], v[:, a:b], scale)
+        acc = part if acc is None else oracle.lse_merge(*acc, *part)
+    return acc
+
+
+@pytest.mark.parametrize("cuts", [[0, 8, 16, 24, 32], [0, 11, 12, 32], [0, 1, 2, 3, 32],
+                                  [0, 0, 32], [0, 32, 32], [0, 5, 5, 20, 32]])
+def test_merge_partition_invariance(cuts):
+    q, k, v = rnd((2, 6, 2, 8), 40, 2.0), rnd((2, 32, 2, 8), 41), rnd((2, 32, 2, 8), 42)
+    o, l = oracle.attention(q, k, v, 0.5)
+    om, lm = merged_over_partition(q, k, v, 0.5, cuts)
+    np.testing.assert_allclose(om, o, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lm, l, atol=1e-12, rtol=0)
+
+
+def test_merge_commutative_associative():
+    parts = [(rnd((1, 5, 2, 3), 50 + i), 3.0 * rnd((1, 2, 5), 60 + i)) for i in range(3)]
+    a, b, c = parts
+    ab = oracle.lse_merge(*a, *b)
+    ba = oracle.lse_merge(*b, *a)
+    np.testing.assert_allclose(ab[0], ba[0], atol=1e-15, rtol=0)
+    np.testing.assert_allclose(ab[1], ba[1], atol=1e-15, rtol=0)
+    left = oracle.lse_merge(*ab, *c)
+    right = oracle.lse_merge(*a, *oracle.lse_merge(*b, *c))
+    np.testing.assert_allclose(left[0], right[0], atol=1e-14, rtol=0)
+    np.testing.assert_allclose(left[1], right[1], atol=1e-14, rtol=0)
+
+
+def test_merge_identity_and_both_empty_exact():
+    o = rnd((1, 4, 2, 3), 70)
+    l = rnd((1, 2, 4), 71)
+    zero = np.zeros_like(o)
+    ninf = np.full_like(l, -np.inf)
+    for om, lm in (oracle.lse_merge(o, l, zero, ninf), oracle.lse_merge(zero, ninf, o, l)):
+        np.testing.assert_array_equal(om, o)
+        np.testing.assert_array_equal(lm, l)
+    om, lm = oracle.lse_merge(zero, ninf, zero, ninf)
+    assert np.all(om == 0) and np.all(np.isneginf(lm)) and not np.any(np.isnan(om))
+
+
+def test_merge_closed_forms():
+    o1, o2 = rnd((1, 3, 1, 2), 72), rnd((1, 3, 1, 2), 73)
+    l = rnd((1, 1, 3), 74)
+    om, lm = oracle.lse_merge(o1, l, o2, l)        # equal weights
+    np.testing.assert_allclose(lm, l + math.log(2), atol=1e-15, rtol=0)
+    np.testing.assert_allclose(om, 0.5 * (o1 + o2), atol=1e-15, rtol=0)
+    om, lm = oracle.lse_merge(o1, l, o2, l + math.log(3))   # weights 1/4, 3/4
+    np.testing.assert_allclose(om, 0.25 * o1 + 0.75 * o2, atol=1e-15, rtol=0)
+    np.testing.assert_allclose(lm, l + math.log(4), atol=1e-14, rtol=0)
+
+
+# ----------------------------------------------------------------------------
+# shard table, ring lap, Ulysses, unified
+# ----------------------------------------------------------------------------
+def test_shard_table():
+    assert oracle.ring_shard_table(4608, 4, False) == [(0, 1152), (1152, 1152), (2304, 1152), (3456, 1152)]
+    assert oracle.ring_shard_table(4607, 3, True) == [(0, 1536), (1536, 1536), (3072, 1535)]
+    assert oracle.ring_shard_table(256, 2, False) == [(0, 128), (128, 128)]
+    with pytest.raises(oracle.NotDivisibleError):
+        oracle.ring_shard_table(4607, 3, False)
+    for S in range(0, 40):
+        for n in range(1, 9):
+            t = oracle.ring_shard_table(S, n, True)
+            lens = [ln for _, ln in t]
+            assert sum(lens) == S and max(lens) - min(lens) <= 1
+            assert all(t[i][0] + t[i][1] == t[i + 1][0] for i in range(n - 1))
+            assert lens == sorted(lens, reverse=True)
+
+
+def test_golden_variant_requirements():
+    spec = json.load(open(os.path.join(GOLDEN, "variant_requirements.json")))
+    q = np.zeros((1, 1, 1, 1))
+    for case in spec["cases"]:
+        S, H = case["S"], case["H"]
+        R, U, ev = case["ring_degree"], case["ulysses_degree"], case["uneven_ok"]
+        # validate without running attention: the same checks cp_attention makes
+        try:
+            if R < 1 or U < 1:
+                raise ValueError
+            if ev and (U != 1 or R < 2):
+                raise oracle.UnsupportedComboError
+            if U > H:
+                got = "invalid_arg"
+                raise StopIteration
+            if U == 1:
+                oracle.ring_shard_table(S, R, ev)
+            elif S % (R * U) or H % U:
+                raise oracle.NotDivisibleError
+            got = "ok"
+        except StopIteration:
+            pass
+        except oracle.NotDivisibleError:
+            got = "not_divisible"
+        except oracle.UnsupportedComboError:
+            got = "unsupported_combo"
+        assert got == case["expect"], case["name"]
+    del q
+
+
+def test_golden_variant_requirements_via_cp_attention():
+    """The same table through the oracle's dispatcher, on tiny shapes with the same divisibility."""
+    spec = json.load(open(os.path.join(GOLDEN, "variant_requirements.json")))
+    for case in spec["cases"]:
+        S, H = case["S"], case["H"]
+        R, U, ev = case["ring_degree"], case["ulysses_degree"], case["uneven_ok"]
+        # shrink S and H but keep S mod 48 and H mod 24, which fix divisibility by every degree used
+        s_small = 48 + S % 48
+        h_small = 24 + H % 24 if U <= 24 else H
+        q = rnd((1, s_small, h_small, 2), 1)
+        try:
+            oracle.cp_attention(q, q, q, 1.0, R, U, ev)
+            got = "ok"
+        except oracle.NotDivisibleError:
+            got = "not_divisible"
+        except oracle.UnsupportedComboError:
+            got = "unsupported_combo"
+        except ValueError:
+            got = "invalid_arg"
+        assert got == case["expect"], case["name"]
+
+
+@pytest.mark.parametrize("S,R,ev", [(24, 2, False), (24, 3, False), (24, 4, False), (23, 3, True),
+                                    (25, 4, True), (5, 4, True), (3, 4, True)])
+def test_ring_equals_full_attention(S, R, ev):
+    q, k, v = rnd((2, S, 2, 4), 80, 1.5), rnd((2, S, 2, 4), 81), rnd((2, S, 2, 4), 82)
+    o, l = oracle.attention(q, k, v, 0.5)
+    orr, lr = oracle.ring_attention(q, k, v, 0.5, R, ev)
+    np.testing.assert_allclose(orr, o, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lr, l, atol=1e-12, rtol=0)
+
+
+def reshape_seq2head(x):
+    U, B, Sl, H, D = x.shape
+    return x.reshape(U, B, Sl, U, H // U, D).transpose(3, 1, 0, 2, 4, 5).reshape(U, B, U * Sl, H // U, D)
+
+
+def test_seq2head_matches_reshape_and_round_trips():
+    x = np.arange(4 * 2 * 3 * 8 * 2).reshape(4, 2, 3, 8, 2)
+    y = oracle.seq2head(x)
+    np.testing.assert_array_equal(y, reshape_seq2head(x))
+    np.testing.assert_array_equal(oracle.head2seq(y), x)
+    # U = 1 is the identity
+    z = np.arange(1 * 2 * 5 * 3 * 2).reshape(1, 2, 5, 3, 2)
+    np.testing.assert_array_equal(oracle.seq2head(z), z)
+    np.testing.assert_array_equal(oracle.head2seq(z), z)
+    # a few explicit elements of the definition
+    U, Sl, Hg = 4, 3, 2
+    for (g, b, s, h, d) in [(0, 0, 0, 0, 0), (3, 1, 11, 1, 1), (2, 0, 7, 0, 1)]:
+        u, sl = divmod(s, Sl)
+        assert y[g, b, s, h, d] == x[u, b, sl, g * Hg + h, d]
+
+
+@pytest.mark.parametrize("U", [1, 2, 4])
+def test_ulysses_equals_full_attention(U):
+    q, k, v = rnd((2, 16, 8, 4), 90, 1.5), rnd((2, 16, 8, 4), 91), rnd((2, 16, 8, 4), 92)
+    o, l = oracle.attention(q, k, v, 0.5)
+    ou, lu = oracle.ulysses_attention(q, k, v, 0.5, U)
+    np.testing.assert_allclose(ou, o, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lu, l, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("R,U", [(2, 2), (2, 4), (4, 2), (3, 2)])
+def test_unified_equals_full_attention(R, U):
+    S = 24
+    q, k, v = rnd((1, S, 4, 4), 93, 1.5), rnd((1, S, 4, 4), 94), rnd((1, S, 4, 4), 95)
+    o, l = oracle.attention(q, k, v, 0.5)
+    ou, lu = oracle.unified_attention(q, k, v, 0.5, R, U)
+    np.testing.assert_allclose(ou, o, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lu, l, atol=1e-12, rtol=0)
+    oc, lc = oracle.cp_attention(q, k, v, 0.5, R, U, False)
+    np.testing.assert_array_equal(oc, ou)
+    np.testing.assert_array_equal(lc, lu)
+
+
+# ----------------------------------------------------------------------------
+# planted mistakes: each mutated copy of an oracle function must fail a pin
+# ----------------------------------------------------------------------------
+def _mut_attention(kind):
+    def f(q, k, v, scale, row_chunk=1024):
+        q, k, v = co._f64(q), co._f64(k), co._f64(v)
+        B, Sq, H, D = q.shape
+        out = np.zeros((B, Sq, H, D)); lse = np.zeros((B, H, Sq))
+        for b in range(B):
+            for h in range(H):
+                hk = (h + 1) % H if kind == "wrong_head" else h
+                kb = k[b, :, hk, :] if kind != "v_for_k" else v[b, :, h, :]
+                s = (1.0 if kind == "no_scale" else scale) * (q[b, :, h, :] @ kb.T)
+                m = s.max(axis=1, keepdims=True)
+                w = np.exp(s - m)
+                l = w.sum(axis=1, keepdims=True)
+                vb = v[b, :, h, :] if kind != "k_for_v" else k[b, :, h, :]
+                out[b, :, h, :] = (w @ vb) / (1.0 if kind == "no_norm" else l)
+                lse[b, h, :] = (np.log(l) if kind == "lse_no_max" else m + np.log(l))[:, 0]
+        return out, lse
+    return f
+
+
+@pytest.mark.parametrize("kind", ["no_scale", "v_for_k", "k_for_v", "no_norm", "lse_no_max", "wrong_head"])
+def test_planted_attention_mistakes_are_caught(kind):
+    q, k, v = rnd((1, 3, 2, 2), 100), rnd((1, 4, 2, 2), 101), rnd((1, 4, 2, 2), 102)
+    o, l = _mut_attention(kind)(q, k, v, 0.7)
+    ob, lb = brute_attention(q, k, v, 0.7)
+    assert max(np.max(np.abs(o - ob)), np.max(np.abs(l - lb))) > 1e-6
+
+
+@pytest.mark.parametrize("kind", ["sign", "no_log", "swap_weights", "max_not_min_guard"])
+def test_planted_merge_mistakes_are_caught(kind, monkeypatch):
+    def bad(out_a, lse_a, out_b, lse_b):
+        m = np.maximum(lse_a, lse_b)
+        tot = np.exp(lse_a - m) + np.exp(lse_b - m)
+        lse = m + (tot if kind == "no_log" else np.log(tot))
+        if kind == "max_not_min_guard":
+            lse = np.minimum(lse_a, lse_b) + np.log(tot)
+        sa = -1.0 if kind == "sign" else 1.0
+        wa = np.exp(sa * (lse_a - lse)); wb = np.exp(lse_b - lse)
+        if kind == "swap_weights":
+            wa, wb = wb, wa
+        return (np.transpose(wa, (0, 2, 1))[..., None] * out_a
+                + np.transpose(wb, (0, 2, 1))[..., None] * out_b), lse
+    monkeypatch.setattr(co, "lse_merge", bad)
+    q, k, v = rnd((1, 4, 1, 4), 103, 2.0), rnd((1, 16, 1, 4), 104), rnd((1, 16, 1, 4), 105)
+    o, l = co.attention(q, k, v, 0.5)
+    om, lm = co.ring_attention(q, k, v, 0.5, 4)
+    assert max(np.max(np.abs(om - o)), np.max(np.abs(lm - l))) > 1e-6
+
+
+@pytest.mark.parametrize("kind", ["head_index", "token_index", "group_swap"])
+def test_planted_permute_mistakes_are_caught(kind):
+    x = np.arange(4 * 1 * 3 * 8 * 2).reshape(4, 1, 3, 8, 2)
+    U, B, Sl, H, D = x.shape
+    Hg = H // U
+    y = np.empty((U, B, Sl * U, Hg, D), dtype=x.dtype)
+    for g in range(U):
+        for u in range(U):
+            for h in range(Hg):
+                src_h = h * U + g if kind == "head_index" else g * Hg + h
+                dst = slice(u * Sl, (u + 1) * Sl) if kind != "token_index" else slice((U - 1 - u) * Sl, (U - u) * Sl)
+                gg = (g + 1) % U if kind == "group_swap" else g
+                y[gg, :, dst, h, :] = x[u, :, :, src_h, :]
+    assert not np.array_equal(y, reshape_seq2head(x))
