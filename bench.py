@@ -1,0 +1,442 @@
+#!/usr/bin/env python3
+"""Throughput of the context-parallel attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--mode fused|stepwise]
+    python bench.py --impl reference ...      # the float64 CPU oracle on the host cores
+
+One step = one cp_attention_fwd over the workload's resident synthetic inputs
+(every row of the hot path: shard table, regroups when Ulysses is on, the
+block-attention lap with its LSE merges). L2 is flushed (a 512 MB write)
+between timed steps, outside the timed events. With N > 1 (torchrun), every
+rank runs its own independent problem on its own GPU (weak scaling, no
+data-path collective); the time is the max over ranks.
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "context-parallel attention fwd TFLOP/s and % bf16 tensor peak on 1 GB300"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_tc_flux_ring4.md")
+TC_KERNEL_SOURCE = os.path.join(ROOT, "context_attention_dits_gb300", "csrc", "attn_tc.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="flux_ring4")
+    ap.add_argument("--mode", default="fused", choices=["fused", "stepwise"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# the oracle on a bounded sample (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """Rank 0's ring lap (attention per block + LSE merge) for `rows` query rows of `heads` heads."""
+
+    def __init__(self, w, q, k, v, rows, heads):
+        import numpy as np
+        import oracle
+        self.oracle, self.w = oracle, w
+        self.table = oracle.ring_shard_table(w.S, w.ring_degree, w.uneven_ok)
+        off0 = self.table[0][0]
+        hs = list(range(heads))
+        self.q = q[:, off0:off0 + rows][:, :, hs].float().numpy().astype(np.float64)
+        self.k = k[:, :, hs].float().numpy().astype(np.float64)
+        self.v = v[:, :, hs].float().numpy().astype(np.float64)
+        self.rows, self.heads = rows, heads
+        self.flops = 4 * w.B * heads * rows * w.S * w.D
+
+    def run(self):
+        o = self.oracle
+        acc = None
+        R = len(self.table)
+        for t in range(R):
+            off, ln = self.table[(0 - t) % R]
+            part = o.attention(self.q, self.k[:, off:off + ln], self.v[:, off:off + ln], self.w.scale)
+            acc = part if acc is None else o.lse_merge(*acc, *part)
+        return acc
+
+    def describe(self):
+        return (f"ring lap of rank 0 for {self.rows} query rows x {self.heads} heads x B={self.w.B} against all "
+                f"{self.w.S} keys ({len(self.table)} blocks), float64 numpy")
+
+
+def sized_sample(w, q, k, v, budget_s, heads_max):
+    """Grow the sample until one run takes about budget_s seconds."""
+    rows, heads = 16, 1
+    while True:
+        s = OracleSample(w, q, k, v, rows, heads)
+        t0 = time.perf_counter()
+        s.run()
+        dt = time.perf_counter() - t0
+        if dt >= budget_s * 0.5 or (rows >= w.S // w.ring_degree and heads >= heads_max):
+            return s, dt
+        grow = max(1.5, min(8.0, budget_s * 0.7 / max(dt, 1e-4)))
+        if rows < w.S // w.ring_degree:
+            rows = min(w.S // w.ring_degree, int(rows * grow) + 1)
+        else:
+            heads = min(heads_max, int(heads * grow) + 1)
+
+
+def cpu_baseline(w, q, k, v, budget_s=12.0):
+    s, _ = sized_sample(w, q, k, v, budget_s / 3, w.H)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        s.run()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s * 0.6 or reps >= 3:
+            break
+    return {"value": s.flops * reps / el / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "sample": s.describe(), "seconds": round(el, 3)}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples, self.proc, self.thread, self.window = [], None, None, None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_id), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append((time.time(), parts))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        t0, t1 = self.window or (0, float("inf"))
+        inside = [p for (t, p) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        if not inside:  # a short timed region: take the samples nearest to it
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside),
+                "power_w_max": max((num(p[2]) or 0.0) for p in inside)}
+
+
+# ---------------------------------------------------------------------------
+# traffic of the dominant kernel from the committed ncu summary
+# ---------------------------------------------------------------------------
+def profiled_traffic(workload, mode):
+    if workload != "flux_ring4" or mode != "fused" or not os.path.exists(PROFILE_SUMMARY):
+        return None
+    text = open(PROFILE_SUMMARY).read()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_sha and m_tr):
+        return None
+    sha = hashlib.sha256(open(TC_KERNEL_SOURCE, "rb").read()).hexdigest()
+    return float(m_tr.group(1)) if sha == m_sha.group(1) else None
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def reduce_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return None
+    from synth import make_qkv
+    q, k, v = make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed, w.q_mult)
+    per_step = max(0.05, 90.0 / max(1, args.steps + args.warmup))
+    s, _ = sized_sample(w, q, k, v, per_step, 1)
+    for _ in range(args.warmup):
+        s.run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        s.run()
+    el = time.perf_counter() - t0
+    val = s.flops * args.steps / el / 1e12
+    line = {"metric": METRIC, "value": val, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w, args.mode),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                             "sample": s.describe()},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    return line
+
+
+def config_of(w, mode):
+    return {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "qkv_dtype": w.dtype,
+            "ring_degree": w.ring_degree, "ulysses_degree": w.ulysses_degree, "uneven_ok": w.uneven_ok,
+            "q_mult": w.q_mult, "lap_mode": mode, "scale": "1/sqrt(D)",
+            "inputs": f"seeded N(0,1) (seed {w.seed}), resident in HBM",
+            "l2": "flushed between timed steps (512 MB write outside the timed events)",
+            "parallelism": f"simulated ring{w.ring_degree} x ulysses{w.ulysses_degree} on one GPU"}
+
+
+def run_ours(args, w, world, rank, local):
+    import numpy as np
+    import torch
+
+    import context_attention_dits_gb300 as cpa
+    from synth import make_qkv
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q_h, k_h, v_h = make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed, w.q_mult)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    mode = args.mode
+    tdt = q.dtype
+    ws_bytes = cpa.cp_attention_workspace_size(w.B, w.H, w.S, w.D, w.ring_degree, w.ulysses_degree, tdt, mode)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    launches_per_step = cpa.cp_attention_launch_count(w.B, w.H, w.S, w.D, w.ring_degree, w.ulysses_degree, tdt,
+                                                      mode)
+
+    def step():
+        cpa.cp_attention_fwd(q, k, v, out, lse, w.scale, w.ring_degree, w.ulysses_degree, w.uneven_ok,
+                             workspace=ws, mode=mode, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = cpa.cp_check_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status after warm-up: {cpa.cp_status_string(status)}")
+
+    # parity spot check of the benchmarked output on a few rows (oracle, rank 0 only)
+    parity = None
+    if rank == 0:
+        import oracle
+        rows = np.sort(np.random.default_rng(0).choice(w.S, size=8, replace=False))
+        ro, rl = oracle.attention_rows(q_h, k_h, v_h, w.scale, rows)
+        go = out[:, rows].double().cpu().numpy()
+        gl = lse[:, :, rows].double().cpu().numpy()
+        err = max(float(np.abs(go - ro).max()), float(np.abs(gl - rl).max()))
+        parity = {"rows_checked": int(len(rows)), "max_abs_err": err, "ok": bool(err <= 1e-2)}
+
+    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[local] if os.environ.get(
+        "CUDA_VISIBLE_DEVICES") else str(local)
+    try:
+        gpu_id = torch.cuda.get_device_properties(dev).uuid
+        gpu_id = f"GPU-{gpu_id}" if not str(gpu_id).startswith("GPU-") else str(gpu_id)
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_id)
+    time.sleep(0.3)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall1 = time.time()
+    clocks.mark(wall0, wall1)
+    time.sleep(0.25)
+    clocks.stop()
+    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = reduce_max(sum(per_step_ms), world)
+    ms_per_step = total_ms / args.steps
+    flops_step = w.flops
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    status = cpa.cp_check_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status after timing: {cpa.cp_status_string(status)}")
+
+    # e2e through host buffers: pinned H2D of q, k, v, the call, D2H of out and lse, all timed
+    q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    out_p = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_p = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (q_p, k_p, v_p))
+    d2h = out_p.numel() * 4 + lse_p.numel() * 4
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(n_e2e):
+        flush.fill_(float(i))
+        e_s[i].record(stream)
+        q.copy_(q_p, non_blocking=True)
+        k.copy_(k_p, non_blocking=True)
+        v.copy_(v_p, non_blocking=True)
+        step()
+        out_p.copy_(out, non_blocking=True)
+        lse_p.copy_(lse, non_blocking=True)
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)), world) / n_e2e
+    e2e_val = world * flops_step / (e2e_ms * 1e-3) / 1e12
+
+    line = None
+    if rank == 0:
+        peaks, peak_src = load_peaks()
+        # dominant kernel: the tensor-core block-attention kernel; in the fused lap it is the
+        # one launch of the step, so its average launch duration is the step's event time
+        if mode == "fused" and w.dtype == "bf16":
+            kernel_ms = ms_per_step
+            per_launch_flops = flops_step
+            scope = "attn_fwd_tc_kernel (one launch per step)"
+        else:
+            kernel_ms = ms_per_step
+            per_launch_flops = flops_step
+            scope = "whole step (several launches; merges and regroups included)"
+        achieved = per_launch_flops / (kernel_ms * 1e-3) / 1e12
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        traffic = profiled_traffic(w.name, mode)
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": traffic, "kernel": scope,
+                    "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed alone)"}
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(w, q_h, k_h, v_h)
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+                "config": config_of(w, mode),
+                "frac_of_bf16_peak": value / world / peak,
+                "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                        "ms_per_step": e2e_ms},
+                "gpu_launches": launches_per_step * args.steps,
+                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks.summary(),
+                "parity_sample": parity,
+                "step_ms_min": min(per_step_ms), "step_ms_median": statistics.median(per_step_ms)}
+    return line
+
+
+def main():
+    args = parse_args()
+    from synth import WORKLOADS
+    w = WORKLOADS[args.workload]
+    world, rank, local = (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+                          int(os.environ.get("LOCAL_RANK", "0")))
+    if args.impl == "reference":
+        if world > 1 and rank != 0:
+            return 0
+        line = run_reference(args, w, world, rank)
+        print(json.dumps(line))
+        return 0
+    world, rank, local = dist_setup()
+    line = run_ours(args, w, world, rank, local)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,491 @@
+// attn_tc.cu — block attention forward on the 5th-generation tensor cores
+// (tcgen05 + TMEM + TMA) for sm_103a, bf16 q/k/v, fp32 (out, lse).
+//
+// What one CTA computes: two 128-row query tiles of one (batch, head) from one
+// simulated rank's shard, against the K/V blocks of that rank's ring lap (or
+// of one ring step), with the online-softmax state (row max m, row sum l,
+// unnormalised output O) carried across K/V tiles and across blocks. Carrying
+// the state across a block boundary is exactly the fp32 LSE merge of the two
+// blocks' (out, lse) partials: with out_a = O_a / l_a and lse_a = m_a + ln l_a,
+//   e^{lse_a - lse} out_a + e^{lse_b - lse} out_b
+//     = (e^{m_a} O_a + e^{m_b} O_b) / (e^{m_a} l_a + e^{m_b} l_b),
+// which is what rescaling O and l to a common maximum computes.
+// (diffusers "Paralelismo de contexto" page, section "Atenção em Anel": each
+// GPU attends to the K/V block it holds, then passes it on; the "Paralelismo"
+// API page, ContextParallelConfig.convert_to_fp32: fp32 output and LSE.)
+//
+// Warp roles (384 threads):
+//   warp 0        TMA producer: Q tiles once, then K and V tiles through a
+//                 two-stage ring each, 128B-swizzled.
+//   warp 1        TMEM allocator and MMA issuer (one thread):
+//                 S_i = Q_i K^T (SS MMA, M=128 N=128 K=16 steps) and
+//                 O_i += P_i V (TS MMA, P read from TMEM), ping-ponging the
+//                 two query tiles so that one tile's softmax overlaps the
+//                 other tile's MMAs.
+//   warps 2-3     idle.
+//   warps 4-7     softmax of query tile 0, warps 8-11 of tile 1: one thread
+//                 per query row (TMEM lane), row max and sum in registers,
+//                 P = 2^(s*scale*log2e - m) rounded to bf16 into TMEM over S,
+//                 O rescaled in TMEM only when the row max grows by more than
+//                 2^8 (the stale maximum is exact: it cancels in O / l).
+//                 Epilogue: O / l staged through shared memory and stored
+//                 coalesced; lse = (m + log2 l) * ln 2.
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D),
+// O_1 [256+D, 256+2D); P_i overwrites the first 64 columns of S_i as packed
+// bf16 pairs.
+// Every wait is bounded (see cp_ptx.cuh); on expiry the CTA drains its
+// in-flight TMA loads and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "cp_internal.h"
+#include "cp_ptx.cuh"
+
+namespace cp {
+
+__device__ uint32_t g_dev_error;  // the device error word (see cp_check_device_status)
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 2^8
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct Smem {
+  static constexpr int kQTile = kTileM * D * 2;   // bytes of one bf16 Q tile
+  static constexpr int kKVTile = kTileN * D * 2;  // bytes of one bf16 K or V tile
+  static constexpr int kHalf = kTileM * 128;      // one 64-column (128-byte) box of a 128-row tile
+  static constexpr int kStages = 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kQTile;
+  static constexpr int kOffV = kOffK + kStages * kKVTile;
+  static constexpr int kOffBar = kOffV + kStages * kKVTile;
+  static constexpr int kNumBars = 16;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 64;
+  // slack to align the base to 1024 bytes; at least 116 KB so that two CTAs
+  // never share an SM (each allocates all 512 TMEM columns)
+  static constexpr int kAlloc = (kBytes + 1024) > 116 * 1024 ? (kBytes + 1024) : 116 * 1024;
+};
+
+// barrier indices
+enum : int {
+  kBarQFull = 0,
+  kBarKFull = 1,   // +stage
+  kBarKEmpty = 3,  // +stage
+  kBarVFull = 5,   // +stage
+  kBarVEmpty = 7,  // +stage
+  kBarSFull = 9,   // +tile
+  kBarPFull = 11,  // +tile
+  kBarOFull = 13,  // +tile
+  kBarDrain = 15,
+};
+
+__device__ __forceinline__ int ring_block(const RingGeom& g, int r, int t) {
+  const int s = g.step >= 0 ? g.step : t;
+  int j = (r - s) % g.n_kv;
+  return j < 0 ? j + g.n_kv : j;
+}
+
+// Walks the K/V tiles of rank r's lap in ring order, skipping empty blocks.
+struct KvCursor {
+  int t, nblk, tile, ntile, off, len;
+  __device__ __forceinline__ void init(const RingGeom& g, int r) {
+    nblk = g.step >= 0 ? 1 : g.n_kv;
+    t = -1;
+    next_block(g, r);
+  }
+  __device__ __forceinline__ void next_block(const RingGeom& g, int r) {
+    tile = 0;
+    while (true) {
+      ++t;
+      if (t >= nblk) return;
+      const int j = ring_block(g, r, t);
+      off = g.kv_off[j];
+      len = g.kv_len[j];
+      ntile = (len + kTileN - 1) / kTileN;
+      if (ntile > 0) return;
+    }
+  }
+  __device__ __forceinline__ int kv0() const { return off + tile * kTileN; }
+  __device__ __forceinline__ int nvalid() const { return min(kTileN, len - tile * kTileN); }
+  __device__ __forceinline__ void advance(const RingGeom& g, int r) {
+    if (++tile >= ntile) next_block(g, r);
+  }
+};
+
+__device__ __forceinline__ int total_tiles(const RingGeom& g, int r) {
+  const int nblk = g.step >= 0 ? 1 : g.n_kv;
+  int n = 0;
+  for (int t = 0; t < nblk; ++t) n += (g.kv_len[ring_block(g, r, t)] + kTileN - 1) / kTileN;
+  return n;
+}
+
+// Bounded wait that ignores the abort flag (used while draining).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ AttnArgs a) {
+  using L = Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_addr(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);  // [0] TMEM base, [1] abort flag
+  volatile uint32_t* abort_flag = misc + 1;
+  auto bar = [&](int i) -> uint32_t { return sb + L::kOffBar + 8 * i; };
+  int blk_h, blk_b;
+
+  // ---- work item: all (tile pair, head, batch) items first, then all
+  // (single tile, head, batch) items; items vary fastest, then heads ----
+  const int n_pairs = a.g.pair_prefix[a.g.n_q];
+  const int n_single = a.g.single_prefix[a.g.n_q];
+  int id = blockIdx.x;
+  int r = 0, qrow0, nq, rows0, rows1;
+  {
+    const int per_hb_pairs = n_pairs;
+    const int64_t pair_ctas = static_cast<int64_t>(n_pairs) * a.H * a.B;
+    int item, h_, b_;
+    if (id < pair_ctas) {
+      item = id % per_hb_pairs;
+      h_ = (id / per_hb_pairs) % a.H;
+      b_ = id / (per_hb_pairs * a.H);
+      while (r + 1 < a.g.n_q && a.g.pair_prefix[r + 1] <= item) ++r;
+      const int lp = item - a.g.pair_prefix[r];
+      qrow0 = a.g.q_off[r] + lp * 2 * kTileM;
+      nq = 2;
+    } else {
+      id -= static_cast<int>(pair_ctas);
+      item = id % n_single;
+      h_ = (id / n_single) % a.H;
+      b_ = id / (n_single * a.H);
+      while (r + 1 < a.g.n_q && a.g.single_prefix[r + 1] <= item) ++r;
+      // the single tile is the last tile of shard r
+      qrow0 = a.g.q_off[r] + (a.g.pair_prefix[r + 1] - a.g.pair_prefix[r]) * 2 * kTileM;
+      nq = 1;
+    }
+    const int rem = a.g.q_off[r] + a.g.q_len[r] - qrow0;
+    rows0 = min(kTileM, rem);
+    rows1 = nq == 2 ? min(kTileM, rem - kTileM) : 0;
+    blk_h = h_;
+    blk_b = b_;
+  }
+  const int h = blk_h, b = blk_b;
+  const int NT = total_tiles(a.g, r);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? 4 : 1);
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(misc), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const uint64_t tmo = a.timeout_ns;
+
+  if (warp == 0) {
+    // ===================== TMA producer =====================
+    if (lane == 0 && NT > 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      int k_issued[2] = {0, 0}, v_issued[2] = {0, 0};
+      mbar_arrive_expect_tx(bar(kBarQFull), nq * L::kQTile);
+      for (int i = 0; i < nq; ++i)
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sb + L::kOffQ + i * L::kQTile + c * L::kHalf, &tq, bar(kBarQFull), c * 64, h,
+                      qrow0 + i * kTileM, b);
+      KvCursor cur;
+      cur.init(a.g, r);
+      for (int it = 0; it < NT; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        if (!mbar_wait_bounded(bar(kBarKEmpty + s), ph ^ 1, abort_flag, a.err, tmo)) break;
+        mbar_arrive_expect_tx(bar(kBarKFull + s), L::kKVTile);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sb + L::kOffK + s * L::kKVTile + c * L::kHalf, &tk, bar(kBarKFull + s), c * 64, h,
+                      cur.kv0(), b);
+        ++k_issued[s];
+        if (!mbar_wait_bounded(bar(kBarVEmpty + s), ph ^ 1, abort_flag, a.err, tmo)) break;
+        mbar_arrive_expect_tx(bar(kBarVFull + s), L::kKVTile);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sb + L::kOffV + s * L::kKVTile + c * L::kHalf, &tv, bar(kBarVFull + s), c * 64, h,
+                      cur.kv0(), b);
+        ++v_issued[s];
+        cur.advance(a.g, r);
+      }
+      if (*abort_flag) {
+        // let every issued copy land before the CTA's shared memory goes away
+        drain_wait(bar(kBarQFull), 0, tmo);
+        for (int s = 0; s < 2; ++s) {
+          if (k_issued[s]) drain_wait(bar(kBarKFull + s), (k_issued[s] - 1) & 1, tmo);
+          if (v_issued[s]) drain_wait(bar(kBarVFull + s), (v_issued[s] - 1) & 1, tmo);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ===================== MMA issuer =====================
+    if (lane == 0 && NT > 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kTileM, kTileN, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kTileM, D, false, true);
+      auto issue_s = [&](int i, int stage) {
+        const uint32_t qa = sb + L::kOffQ + i * L::kQTile;
+        const uint32_t ka = sb + L::kOffK + stage * L::kKVTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kHalf + (kk & 3) * 32;
+          mma_ss(tmem + i * kTileN, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                 idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int i, int stage, bool acc) {
+        const uint32_t va = sb + L::kOffV + stage * L::kKVTile;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          mma_ts(tmem + 256 + i * D, tmem + i * kTileN + kk * 8, smem_desc_sw128(va + kk * 2048, L::kHalf, 1024),
+                 idesc_o, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait_bounded(bar(kBarQFull), 0, abort_flag, a.err, tmo) &&
+                mbar_wait_bounded(bar(kBarKFull), 0, abort_flag, a.err, tmo);
+      if (ok) {
+        tc_fence_after();
+        for (int i = 0; i < nq; ++i) {
+          issue_s(i, 0);
+          mma_commit(bar(kBarSFull + i));
+        }
+        mma_commit(bar(kBarKEmpty));
+      }
+      for (int it = 0; ok && it < NT; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        if (!mbar_wait_bounded(bar(kBarVFull + s), ph, abort_flag, a.err, tmo)) { ok = false; break; }
+        for (int i = 0; i < nq; ++i) {
+          if (!mbar_wait_bounded(bar(kBarPFull + i), it & 1, abort_flag, a.err, tmo)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(i, s, it > 0);
+          if (it == NT - 1) mma_commit(bar(kBarOFull + i));
+          if (i == nq - 1) mma_commit(bar(kBarVEmpty + s));
+          if (it + 1 < NT) {
+            const int s2 = (it + 1) & 1;
+            if (i == 0) {
+              if (!mbar_wait_bounded(bar(kBarKFull + s2), ((it + 1) >> 1) & 1, abort_flag, a.err, tmo)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            issue_s(i, s2);
+            mma_commit(bar(kBarSFull + i));
+            if (i == nq - 1) mma_commit(bar(kBarKEmpty + s2));
+          }
+        }
+      }
+      if (!ok) {
+        mma_commit(bar(kBarDrain));
+        drain_wait(bar(kBarDrain), 0, tmo);
+      }
+    }
+  } else if (warp >= 4) {
+    // ===================== softmax + epilogue =====================
+    const int i = (warp - 4) >> 2;  // query tile of this warpgroup
+    const int wq = warp & 3;        // TMEM lane quadrant of this warp
+    const int row = wq * 32 + lane;
+    if (i < nq) {
+      const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+      const uint32_t t_s = tmem + lane_off + i * kTileN;
+      const uint32_t t_o = tmem + lane_off + 256 + i * D;
+      const float sl2 = a.scale_log2;
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      KvCursor cur;
+      cur.init(a.g, r);
+      for (int it = 0; it < NT; ++it) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarSFull + i), it & 1, abort_flag, a.err, tmo));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[kTileN];
+#pragma unroll
+        for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        tmem_wait_ld();
+        const int nv = cur.nvalid();
+        if (nv < kTileN) {
+#pragma unroll
+          for (int c = 0; c < kTileN; ++c)
+            if (c >= nv) sr[c] = __float_as_uint(-INFINITY);
+        }
+        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+        for (int c = 4; c < kTileN; c += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+          mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+        }
+        const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const bool need = mxs > m_used + kRescaleThreshold;
+        const bool warp_rescale = __any_sync(0xffffffffu, need);
+        float f = 1.f;
+        if (need) {
+          f = ex2_approx(m_used - mxs);  // 0 on the first tile (m_used = -inf)
+          m_used = mxs;
+        }
+        // P = 2^(s*scale*log2e - m_used), bf16, over the first 64 columns of S
+        const float nm = -m_used;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e]), sl2, nm));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e + 1]), sl2, nm));
+            ls[(2 * e) & 3] += p0;
+            ls[(2 * e + 1) & 3] += p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(t_s + half * 32, pk);
+        }
+        l = l * f + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+        // O is idle here: PV of the previous tile completed before S of this
+        // tile was committed, and PV of this tile waits for P.
+        if (warp_rescale && it > 0) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st32(t_o + c * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarPFull + i));
+        cur.advance(a.g, r);
+      }
+      if (ok && NT > 0) ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarOFull + i), 0, abort_flag, a.err, tmo));
+      if (ok) {
+        tc_fence_after();
+        const int rows_valid = i == 0 ? rows0 : rows1;
+        const int tok0 = qrow0 + i * kTileM;  // first token of this tile
+        const float inv_l = NT > 0 ? 1.f / l : 0.f;
+        const float lse_v = NT > 0 ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if (row < rows_valid) a.lse[b * a.l_bstride + h * a.l_hstride + tok0 + row] = lse_v;
+        // stage 32 rows x 32 fp32 per warp in this tile's (now idle) Q buffer, 128B-swizzled,
+        // then store 4 rows x 128 contiguous bytes per warp instruction
+        float* stage = reinterpret_cast<float*>(smem + L::kOffQ + i * L::kQTile + wq * 4096);
+        float* out_b = a.out + b * a.o_bstride + static_cast<int64_t>(h) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          if (NT > 0) {
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float4 val = make_float4(__uint_as_float(o[4 * q4]) * inv_l, __uint_as_float(o[4 * q4 + 1]) * inv_l,
+                                     __uint_as_float(o[4 * q4 + 2]) * inv_l, __uint_as_float(o[4 * q4 + 3]) * inv_l);
+            *reinterpret_cast<float4*>(stage + lane * 32 + ((q4 ^ (lane & 7)) * 4)) = val;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int pass = 0; pass < 8; ++pass) {
+            const int rr = pass * 4 + (lane >> 3);
+            const int q4 = lane & 7;
+            const float4 val = *reinterpret_cast<const float4*>(stage + rr * 32 + ((q4 ^ (rr & 7)) * 4));
+            const int grow = wq * 32 + rr;
+            if (grow < rows_valid)
+              *reinterpret_cast<float4*>(out_b + static_cast<int64_t>(tok0 + grow) * a.o_sstride + c * 32 + q4 * 4) = val;
+          }
+          __syncwarp();
+        }
+      }
+    }
+  }
+
+  // ---- teardown: every thread of the CTA arrives here, aborted or not ----
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// A kernel that exercises the bounded wait on a barrier that nothing
+// completes: every thread times out, the first raises the error word.
+__global__ void wait_probe_kernel(uint32_t* err, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar_storage;
+  __shared__ uint32_t abort_word;
+  const uint32_t bar = smem_addr(&bar_storage);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    abort_word = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  (void)mbar_wait_bounded(bar, 0, &abort_word, err, timeout_ns);
+  __syncthreads();
+}
+
+template <int D>
+cudaError_t launch_tc_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        cudaStream_t s) {
+  using L = Smem<D>;
+  static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int64_t items = static_cast<int64_t>(a.g.pair_prefix[a.g.n_q] + a.g.single_prefix[a.g.n_q]) * a.H * a.B;
+  if (items == 0) return cudaSuccess;
+  if (items > 0x7fffffff) return cudaErrorInvalidValue;
+  attn_fwd_tc_kernel<D><<<dim3(static_cast<unsigned>(items)), kThreads, L::kAlloc, s>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+uint32_t* device_error_word() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) return nullptr;
+  return static_cast<uint32_t*>(p);
+}
+
+cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           cudaStream_t s) {
+  if (a.D == 64) return launch_tc_d<64>(a, tq, tk, tv, s);
+  if (a.D == 128) return launch_tc_d<128>(a, tq, tk, tv, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_wait_probe(uint32_t* err, uint64_t timeout_ns, cudaStream_t s) {
+  wait_probe_kernel<<<1, 64, 0, s>>>(err, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace cp

@@ -1,0 +1,456 @@
+// cp_api.cu — the C ABI of libcpattn.so (declared in include/cp_attn.h):
+// argument validation, the ring shard table, tensor-map set-up, and the host
+// driver that sequences the regroup, block-attention and merge launches of a
+// simulated context-parallel attention forward on one GPU.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "cp_attn.h"
+#include "cp_internal.h"
+
+namespace {
+
+using cp::AttnArgs;
+using cp::RingGeom;
+using cp::SegCopy;
+
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s per device-side wait
+constexpr int kMaxDevices = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------
+// device checks and per-device cached lookups
+// ---------------------------------------------------------------------------
+struct DeviceInfo {
+  int checked = 0;  // 0 unknown, 1 sm_103, -1 other
+  uint32_t* err = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+cp_status current_device(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CP_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.checked == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return CP_ERR_CUDA;
+    d.checked = (major == 10 && minor == 3) ? 1 : -1;
+    if (d.checked == 1) {
+      d.err = cp::device_error_word();
+      if (!d.err) {
+        d.checked = 0;
+        return CP_ERR_CUDA;
+      }
+    }
+  }
+  if (d.checked != 1) return CP_ERR_UNSUPPORTED_DEVICE;
+  *out = &d;
+  return CP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// TMA tensor maps (driver entry point fetched through the runtime, so the
+// library links no libcuda and loads on machines without a GPU driver)
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// bf16 [Bn, S, H, D] with batch stride bstride elements; box = 64 columns x
+// 128 tokens of one head, 128-byte swizzle (the K-major operand layout the
+// MMA descriptors expect).
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int D, int H, int S, int Bn, int64_t bstride) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(Bn)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                           static_cast<cuuint64_t>(bstride) * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(cp::kTileM), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// shard table: balanced split (first S mod n shards one token longer)
+// ---------------------------------------------------------------------------
+cp_status shard_table(int S, int n, bool uneven_ok, int* off, int* len) {
+  if (n < 1 || S < 0) return CP_ERR_INVALID_ARG;
+  const int base = S / n, extra = S % n;
+  if (extra && !uneven_ok) return CP_ERR_NOT_DIVISIBLE;
+  int o = 0;
+  for (int r = 0; r < n; ++r) {
+    off[r] = o;
+    len[r] = base + (r < extra ? 1 : 0);
+    o += len[r];
+  }
+  return CP_OK;
+}
+
+void fill_geom(RingGeom* g, cp_dtype dt, int nq, const int* qoff, const int* qlen, int nkv, const int* kvoff,
+               const int* kvlen, int step) {
+  std::memset(g, 0, sizeof(*g));
+  (void)dt;
+  g->n_q = nq;
+  for (int r = 0; r < nq; ++r) {
+    g->q_off[r] = qoff[r];
+    g->q_len[r] = qlen[r];
+    g->cta_prefix[r + 1] = g->cta_prefix[r] + cp::f32_items_for_rows(qlen[r]);
+    g->pair_prefix[r + 1] = g->pair_prefix[r] + cp::tc_pairs_for_rows(qlen[r]);
+    g->single_prefix[r + 1] = g->single_prefix[r] + cp::tc_singles_for_rows(qlen[r]);
+  }
+  g->n_kv = nkv;
+  for (int j = 0; j < nkv; ++j) {
+    g->kv_off[j] = kvoff[j];
+    g->kv_len[j] = kvlen[j];
+  }
+  g->step = step;
+}
+
+// One attention launch over tensors q [Bn, Sq, H, D], k/v [Bn, Skv, H, D].
+struct AttnTensors {
+  const void* q;
+  const void* k;
+  const void* v;
+  int Bn, H, D, Sq, Skv;
+  int64_t q_bstride, kv_bstride;
+  float* out;
+  int64_t o_bstride;
+  float* lse;  // dense [Bn, H, Sq]
+};
+
+cp_status launch_attention(const AttnTensors& t, const RingGeom& g, float scale, cp_dtype dt, DeviceInfo* dev,
+                           cudaStream_t s) {
+  AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.g = g;
+  a.B = t.Bn;
+  a.H = t.H;
+  a.D = t.D;
+  a.scale = scale;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.out = t.out;
+  a.o_bstride = t.o_bstride;
+  a.o_sstride = static_cast<int64_t>(t.H) * t.D;
+  a.lse = t.lse;
+  a.l_bstride = static_cast<int64_t>(t.H) * t.Sq;
+  a.l_hstride = t.Sq;
+  a.err = dev->err;
+  a.timeout_ns = kWaitTimeoutNs;
+  cudaError_t e;
+  if (dt == CP_BF16) {
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap_bf16(&tq, t.q, t.D, t.H, t.Sq, t.Bn, t.q_bstride)) return CP_ERR_CUDA;
+    const bool kv_empty = t.Skv == 0;
+    if (!make_tmap_bf16(&tk, kv_empty ? t.q : t.k, t.D, t.H, kv_empty ? t.Sq : t.Skv, t.Bn,
+                        kv_empty ? t.q_bstride : t.kv_bstride))
+      return CP_ERR_CUDA;
+    if (!make_tmap_bf16(&tv, kv_empty ? t.q : t.v, t.D, t.H, kv_empty ? t.Sq : t.Skv, t.Bn,
+                        kv_empty ? t.q_bstride : t.kv_bstride))
+      return CP_ERR_CUDA;
+    e = cp::launch_attn_tc(a, tq, tk, tv, s);
+  } else {
+    a.qf = static_cast<const float*>(t.q);
+    a.kf = static_cast<const float*>(t.k);
+    a.vf = static_cast<const float*>(t.v);
+    a.q_bstride = t.q_bstride;
+    a.q_sstride = static_cast<int64_t>(t.H) * t.D;
+    a.kv_bstride = t.kv_bstride;
+    a.kv_sstride = static_cast<int64_t>(t.H) * t.D;
+    e = cp::launch_attn_f32(a, s);
+  }
+  return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+int elem_size(cp_dtype dt) { return dt == CP_BF16 ? 2 : 4; }
+
+cp_status check_common(int B, int H, int S, int D, cp_dtype dt) {
+  if (B < 0 || H < 1 || S < 0) return CP_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return CP_ERR_INVALID_ARG;
+  if (dt != CP_BF16 && dt != CP_F32) return CP_ERR_INVALID_ARG;
+  return CP_OK;
+}
+
+// Workspace layout of cp_attention_fwd (every piece 256-byte aligned):
+// [q_h | k_h | v_h] (Ulysses regroups of the inputs), [out_h | lse_h] (the
+// head-sharded result), [out_p | lse_p] (one ring step's partial).
+struct WsLayout {
+  size_t qh = 0, kh = 0, vh = 0, oh = 0, lh = 0, op = 0, lp = 0, total = 0;
+};
+
+WsLayout ws_layout(int B, int H, int S, int D, int R, int U, cp_dtype dt, cp_lap_mode mode) {
+  WsLayout w;
+  const size_t n = static_cast<size_t>(B) * S * H * D;
+  const size_t nl = static_cast<size_t>(B) * H * S;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = round_up(o + bytes, 256);
+    return at;
+  };
+  if (U > 1) {
+    w.qh = take(n * elem_size(dt));
+    w.kh = take(n * elem_size(dt));
+    w.vh = take(n * elem_size(dt));
+    w.oh = take(n * 4);
+    w.lh = take(nl * 4);
+  }
+  if (mode == CP_LAP_STEPWISE && R > 1) {
+    w.op = take(n * 4);
+    w.lp = take(nl * 4);
+  }
+  w.total = o;
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cp_status_string(cp_status s) {
+  switch (s) {
+    case CP_OK: return "ok";
+    case CP_ERR_INVALID_ARG: return "invalid argument";
+    case CP_ERR_NOT_DIVISIBLE: return "sequence length or head count not divisible by the parallel degree";
+    case CP_ERR_UNSUPPORTED_COMBO: return "unsupported combination of parallel degrees and flags";
+    case CP_ERR_ALIGNMENT: return "pointer or stride not 16-byte aligned";
+    case CP_ERR_CUDA: return "CUDA error";
+    case CP_ERR_TIMEOUT: return "device-side wait timed out";
+    case CP_ERR_WORKSPACE: return "workspace missing or too small";
+    case CP_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103 (GB300)";
+  }
+  return "unknown status";
+}
+
+int cp_version(void) { return 10000; }
+
+cp_status cp_block_attn_fwd(const void* q, const void* k, const void* v, float* out, float* lse, int B, int H, int Sq,
+                            int Skv, int D, float scale, int64_t q_bstride, int64_t kv_bstride, int64_t o_bstride,
+                            cp_dtype dt, void* stream) {
+  cp_status st = check_common(B, H, Sq, D, dt);
+  if (st != CP_OK) return st;
+  if (Skv < 0 || !std::isfinite(scale)) return CP_ERR_INVALID_ARG;
+  const int64_t row = static_cast<int64_t>(H) * D;
+  if (q_bstride == 0) q_bstride = Sq * row;
+  if (kv_bstride == 0) kv_bstride = Skv * row;
+  if (o_bstride == 0) o_bstride = Sq * row;
+  if (q_bstride < Sq * row || kv_bstride < Skv * row || o_bstride < Sq * row) return CP_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0) return CP_OK;
+  if (!q || !out || !lse || (Skv > 0 && (!k || !v))) return CP_ERR_INVALID_ARG;
+  const int eb = elem_size(dt);
+  if (!aligned16(q) || !aligned16(out) || !aligned16(lse) || (Skv > 0 && (!aligned16(k) || !aligned16(v))) ||
+      (q_bstride * eb) % 16 || (kv_bstride * eb) % 16 || (o_bstride * 4) % 16)
+    return CP_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev)) != CP_OK) return st;
+  const int zero = 0;
+  RingGeom g;
+  fill_geom(&g, dt, 1, &zero, &Sq, 1, &zero, &Skv, 0);
+  AttnTensors t{q, k, v, B, H, D, Sq, Skv, q_bstride, kv_bstride, out, o_bstride, lse};
+  return launch_attention(t, g, scale, dt, dev, static_cast<cudaStream_t>(stream));
+}
+
+cp_status cp_lse_merge(float* out_acc, float* lse_acc, const float* out_blk, const float* lse_blk, int B, int H, int S,
+                       int D, void* stream) {
+  if (B < 0 || H < 1 || S < 0 || D < 4 || D % 4) return CP_ERR_INVALID_ARG;
+  if (B == 0 || S == 0) return CP_OK;
+  if (!out_acc || !lse_acc || !out_blk || !lse_blk) return CP_ERR_INVALID_ARG;
+  if (!aligned16(out_acc) || !aligned16(out_blk) || (reinterpret_cast<uintptr_t>(lse_acc) & 3) ||
+      (reinterpret_cast<uintptr_t>(lse_blk) & 3))
+    return CP_ERR_ALIGNMENT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CP_ERR_CUDA;
+  return cp::launch_lse_merge(out_acc, lse_acc, out_blk, lse_blk, B, H, S, D, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? CP_OK
+             : CP_ERR_CUDA;
+}
+
+static cp_status check_permute(const void* in, const void* out, int U, int B, int S, int H, int D, int eb) {
+  if (U < 1 || B < 0 || S < 0 || H < 1 || D < 1 || (eb != 1 && eb != 2 && eb != 4 && eb != 8))
+    return CP_ERR_INVALID_ARG;
+  if (U > H || H % U || S % U) return CP_ERR_INVALID_ARG;
+  if (B > 0 && S > 0 && (!in || !out)) return CP_ERR_INVALID_ARG;
+  return CP_OK;
+}
+
+cp_status cp_ulysses_seq2head(const void* in, void* out, int U, int B, int S, int H, int D, int elem_bytes,
+                              void* stream) {
+  cp_status st = check_permute(in, out, U, B, S, H, D, elem_bytes);
+  if (st != CP_OK) return st;
+  if (B == 0 || S == 0) return CP_OK;
+  const int64_t Sl = S / U, Hg = H / U;
+  // out segments (g, b, u, s) of Hg*D elements <- in[u][b, s, g*Hg : (g+1)*Hg, :]
+  SegCopy c{in, out, U, B, U, Sl, Hg * D, Sl * H * D, static_cast<int64_t>(B) * Sl * H * D, H * D,
+            Hg * D, elem_bytes};
+  return cp::launch_segment_copy(c, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+cp_status cp_ulysses_head2seq(const void* in, void* out, int U, int B, int S, int H, int D, int elem_bytes,
+                              void* stream) {
+  cp_status st = check_permute(in, out, U, B, S, H, D, elem_bytes);
+  if (st != CP_OK) return st;
+  if (B == 0 || S == 0) return CP_OK;
+  const int64_t Sl = S / U, Hg = H / U;
+  // out segments (u, b, s, g) of Hg*D elements <- in[g][b, u*Sl + s, :, :]
+  SegCopy c{in, out, U, B, Sl, U, Sl * Hg * D, static_cast<int64_t>(S) * Hg * D, Hg * D,
+            static_cast<int64_t>(B) * S * Hg * D, Hg * D, elem_bytes};
+  return cp::launch_segment_copy(c, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+cp_status cp_attention_validate(int B, int H, int S, int D, int ring_degree, int ulysses_degree, int uneven_ok,
+                                cp_dtype dt) {
+  cp_status st = check_common(B, H, S, D, dt);
+  if (st != CP_OK) return st;
+  const int R = ring_degree, U = ulysses_degree;
+  if (R < 1 || U < 1 || R > cp::kMaxRanks) return CP_ERR_INVALID_ARG;
+  if (uneven_ok && (U != 1 || R < 2)) return CP_ERR_UNSUPPORTED_COMBO;
+  if (U > H) return CP_ERR_INVALID_ARG;
+  if (U == 1) return (S % R && !uneven_ok) ? CP_ERR_NOT_DIVISIBLE : CP_OK;
+  if (H % U || S % (static_cast<int64_t>(R) * U)) return CP_ERR_NOT_DIVISIBLE;
+  return CP_OK;
+}
+
+cp_status cp_ring_shard_table(int S, int n, int uneven_ok, int* offsets, int* lengths) {
+  if (!offsets || !lengths) return CP_ERR_INVALID_ARG;
+  return shard_table(S, n, uneven_ok != 0, offsets, lengths);
+}
+
+size_t cp_attention_workspace_size(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt,
+                                   cp_lap_mode mode) {
+  if (B < 0 || H < 1 || S < 0 || D < 1 || ring_degree < 1 || ulysses_degree < 1) return 0;
+  return ws_layout(B, H, S, D, ring_degree, ulysses_degree, dt, mode).total;
+}
+
+int cp_attention_launch_count(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt,
+                              cp_lap_mode mode) {
+  (void)H;
+  (void)D;
+  (void)dt;
+  if (B == 0 || S == 0) return 0;
+  const int R = ring_degree, U = ulysses_degree;
+  int n = (mode == CP_LAP_STEPWISE && R > 1) ? R + (R - 1) : 1;
+  if (U > 1) n += 3 /* seq2head q, k, v */ + 2 /* head2seq out, lse */;
+  return n;
+}
+
+cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* out, float* lse, int B, int H, int S,
+                           int D, float scale, int ring_degree, int ulysses_degree, int uneven_ok, void* workspace,
+                           size_t ws_bytes, cp_dtype dt, cp_lap_mode mode, void* stream) {
+  cp_status st = cp_attention_validate(B, H, S, D, ring_degree, ulysses_degree, uneven_ok, dt);
+  if (st != CP_OK) return st;
+  if (!std::isfinite(scale) || (mode != CP_LAP_FUSED && mode != CP_LAP_STEPWISE)) return CP_ERR_INVALID_ARG;
+  if (B == 0 || S == 0) return CP_OK;
+  if (!q || !k || !v || !out || !lse) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return CP_ERR_ALIGNMENT;
+  const int R = ring_degree, U = ulysses_degree;
+  const WsLayout w = ws_layout(B, H, S, D, R, U, dt, mode);
+  if (w.total > 0 && (!workspace || ws_bytes < w.total)) return CP_ERR_WORKSPACE;
+  if (w.total > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255)) return CP_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev)) != CP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const int eb = elem_size(dt);
+  const int Hg = H / U, Bn = B * U;
+  const int64_t row = static_cast<int64_t>(Hg) * D;
+
+  // --- Ulysses all-to-all #1 (simulated): global [B,S,H,D] -> [U][B,S,H/U,D] ---
+  const void *qa = q, *ka = k, *va = v;
+  float* oa = out;
+  float* la = lse;
+  if (U > 1) {
+    void* dst[3] = {ws + w.qh, ws + w.kh, ws + w.vh};
+    const void* src[3] = {q, k, v};
+    for (int i = 0; i < 3; ++i) {
+      // out segments (g, b, t) of Hg*D elements <- in[b, t, g*Hg : (g+1)*Hg, :]
+      SegCopy c{src[i], dst[i], 1, U, B, S, 0, row, static_cast<int64_t>(S) * H * D,
+                static_cast<int64_t>(H) * D, row, eb};
+      if (cp::launch_segment_copy(c, s) != cudaSuccess) return CP_ERR_CUDA;
+    }
+    qa = dst[0];
+    ka = dst[1];
+    va = dst[2];
+    oa = reinterpret_cast<float*>(ws + w.oh);
+    la = reinterpret_cast<float*>(ws + w.lh);
+  }
+
+  // --- ring lap over R simulated ranks on every (group, batch) entry ---
+  int off[cp::kMaxRanks], len[cp::kMaxRanks];
+  if ((st = shard_table(S, R, uneven_ok != 0, off, len)) != CP_OK) return st;
+  const int64_t bstride = S * row;
+  if (mode == CP_LAP_FUSED || R == 1) {
+    RingGeom g;
+    fill_geom(&g, dt, R, off, len, R, off, len, -1);
+    AttnTensors t{qa, ka, va, Bn, Hg, D, S, S, bstride, bstride, oa, bstride, la};
+    if ((st = launch_attention(t, g, scale, dt, dev, s)) != CP_OK) return st;
+  } else {
+    float* op = reinterpret_cast<float*>(ws + w.op);
+    float* lp = reinterpret_cast<float*>(ws + w.lp);
+    for (int step = 0; step < R; ++step) {
+      RingGeom g;
+      fill_geom(&g, dt, R, off, len, R, off, len, step);
+      AttnTensors t{qa, ka, va, Bn, Hg, D, S, S, bstride, bstride, step == 0 ? oa : op, bstride, step == 0 ? la : lp};
+      if ((st = launch_attention(t, g, scale, dt, dev, s)) != CP_OK) return st;
+      if (step > 0 && cp::launch_lse_merge(oa, la, op, lp, Bn, Hg, S, D, s) != cudaSuccess) return CP_ERR_CUDA;
+    }
+  }
+
+  // --- Ulysses all-to-all #2 (simulated): [U][B,S,H/U,D] -> [B,S,H,D]; lse [U][B,H/U,S] -> [B,H,S] ---
+  if (U > 1) {
+    SegCopy co{oa, out, 1, B, S, U, 0, bstride, row, static_cast<int64_t>(B) * bstride, row, 4};
+    if (cp::launch_segment_copy(co, s) != cudaSuccess) return CP_ERR_CUDA;
+    SegCopy cl{la, lse, 1, B, U, Hg, 0, static_cast<int64_t>(Hg) * S, static_cast<int64_t>(B) * Hg * S, S, S, 4};
+    if (cp::launch_segment_copy(cl, s) != cudaSuccess) return CP_ERR_CUDA;
+  }
+  return CP_OK;
+}
+
+cp_status cp_check_device_status(void* stream) {
+  DeviceInfo* dev = nullptr;
+  cp_status st = current_device(&dev);
+  if (st != CP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CP_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, dev->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return CP_ERR_CUDA;
+  if (word == 0) return CP_OK;
+  if (cudaMemset(dev->err, 0, sizeof(word)) != cudaSuccess) return CP_ERR_CUDA;
+  return CP_ERR_TIMEOUT;
+}
+
+cp_status cp_debug_bounded_wait_probe(int timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return CP_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  cp_status st = current_device(&dev);
+  if (st != CP_OK) return st;
+  return cp::launch_wait_probe(dev->err, static_cast<uint64_t>(timeout_us) * 1000ull,
+                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? CP_OK
+             : CP_ERR_CUDA;
+}
+
+}  // extern "C"

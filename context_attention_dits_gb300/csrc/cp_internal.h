@@ -1,0 +1,92 @@
+// cp_internal.h — launch parameters shared by the kernels and the host driver
+// of libcpattn.so. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace cp {
+
+constexpr int kMaxRanks = 16;       // largest ring degree the launch tables hold
+constexpr int kTileM = 128;         // query rows per tensor-core tile
+constexpr int kTileN = 128;         // keys per K/V tile
+
+// Ring geometry of one launch: the query shards (one per simulated rank) and
+// the K/V blocks they visit. Rank r at ring step t attends to block
+// (r - t) mod n_kv: its own block first, then the one "received" from its
+// predecessor. step >= 0 restricts a launch to that single step; step < 0
+// runs the whole lap inside the launch.
+struct RingGeom {
+  int n_q;
+  int q_off[kMaxRanks];
+  int q_len[kMaxRanks];
+  int cta_prefix[kMaxRanks + 1];   // CUDA-core kernel: 8-row work items per shard, prefix sums
+  int pair_prefix[kMaxRanks + 1];  // tensor-core kernel: items with two 128-row Q tiles, prefix sums
+  int single_prefix[kMaxRanks + 1];  // tensor-core kernel: items with one Q tile (odd tile count)
+  int n_kv;
+  int kv_off[kMaxRanks];
+  int kv_len[kMaxRanks];
+  int step;
+};
+
+struct AttnArgs {
+  RingGeom g;
+  int B;   // batch entries (Ulysses head groups folded in)
+  int H;   // heads per batch entry
+  int D;   // head dim
+  float scale;       // softmax scale applied to q.k
+  float scale_log2;  // scale * log2(e)
+  // outputs: out[b*o_bstride + s*o_sstride + h*D + d], lse[b*l_bstride + h*l_hstride + s]
+  float* out;
+  int64_t o_bstride, o_sstride;
+  float* lse;
+  int64_t l_bstride, l_hstride;
+  // raw inputs (element strides) for the CUDA-core fp32 path
+  const float* qf;
+  const float* kf;
+  const float* vf;
+  int64_t q_bstride, q_sstride, kv_bstride, kv_sstride;
+  // device error word and the bound on each device-side wait
+  uint32_t* err;
+  uint64_t timeout_ns;
+};
+
+// Tensor-core work items of a shard of `rows` query rows: tile pairs, plus one
+// single tile when the tile count is odd. All pairs of all shards are launched
+// before all singles, so the short items fill the last wave.
+inline int tc_tiles_for_rows(int rows) { return (rows + kTileM - 1) / kTileM; }
+inline int tc_pairs_for_rows(int rows) { return tc_tiles_for_rows(rows) / 2; }
+inline int tc_singles_for_rows(int rows) { return tc_tiles_for_rows(rows) % 2; }
+// Work items per shard for the CUDA-core kernel: 8 query rows per CTA.
+constexpr int kF32RowsPerCta = 8;
+inline int f32_items_for_rows(int rows) { return (rows + kF32RowsPerCta - 1) / kF32RowsPerCta; }
+
+// Launchers (each returns the launch error, cudaSuccess if none).
+cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, cudaStream_t s);
+cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_lse_merge(float* out_acc, float* lse_acc, const float* out_blk, const float* lse_blk,
+                             int B, int H, int S, int D, cudaStream_t s);
+
+// Copy of n0*n1*n2*n3 segments of seg_elems elements each: output segments are
+// contiguous in (i0, i1, i2, i3) order; the input segment (i0, i1, i2, i3)
+// starts at element i0*st0 + i1*st1 + i2*st2 + i3*st3.
+struct SegCopy {
+  const void* in;
+  void* out;
+  int64_t n0, n1, n2, n3;
+  int64_t st0, st1, st2, st3;
+  int64_t seg_elems;
+  int elem_bytes;
+};
+// Picks the widest vector (16, 8, 4 or 1 bytes) that every segment start, the
+// segment length and both base pointers allow.
+cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s);
+
+// Device error word of the tensor-core kernel's translation unit.
+uint32_t* device_error_word();  // device address on the current device, or nullptr
+cudaError_t launch_wait_probe(uint32_t* err, uint64_t timeout_ns, cudaStream_t s);
+
+}  // namespace cp

@@ -1,0 +1,210 @@
+/*
+ * cp_attn.h — C ABI of libcpattn.so: context-parallel attention forward for
+ * diffusion transformers on one GB300 (sm_103a).
+ *
+ * What it computes (diffusers documentation, "Paralelismo de contexto" page,
+ * sections "Atenção em Anel", "Atenção Ulysses", "Atenção Unificada",
+ * "Ring Anything Attention", and the "Paralelismo" API page,
+ * ContextParallelConfig): non-causal softmax attention of a query shard
+ * against the key/value blocks of a ring lap, each block returning an fp32
+ * (output, log-sum-exp) partial that is merged online, so that one full lap
+ * equals full attention; plus the Ulysses all-to-all regroups between a
+ * sequence-sharded and a head-sharded layout. The ranks of the ring and of the
+ * Ulysses groups are simulated as shards of one buffer on one GPU: a block
+ * "received" from another rank is a pointer offset, and the all-to-all is a
+ * regroup kernel that moves the same bytes.
+ *
+ * Conventions shared by every call
+ *   - Layouts: q, k, v, out are [B, S, H, D] row-major (D contiguous, then H,
+ *     then S, then B); lse is [B, H, S] float32, natural logarithm of the sum
+ *     of exp over the scaled logits scale * q.k. Non-causal, no mask.
+ *   - Pointers are DEVICE pointers unless stated. The caller owns every buffer
+ *     (inputs, outputs, workspace); the library allocates no device memory
+ *     and keeps no per-call state. Outputs must not alias inputs unless stated.
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call is asynchronous on that stream. Arguments are validated on
+ *     the host before anything is launched; a failed validation launches
+ *     nothing and returns a negative cp_status.
+ *   - Supported: D in {64, 128}; q/k/v dtype bf16 (tensor-core path) or f32
+ *     (CUDA-core path); out and lse always float32.
+ *   - Alignment: every pointer 16-byte aligned; batch strides such that each
+ *     batch starts 16-byte aligned. Otherwise CP_ERR_ALIGNMENT.
+ *   - Device-side waits are bounded. A kernel whose wait expires records it in
+ *     a device error word, releases its resources and returns; read it with
+ *     cp_check_device_status().
+ */
+#ifndef CP_ATTN_H_
+#define CP_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARG = -1,       /* bad size, null pointer, unsupported D or dtype, degree > heads */
+  CP_ERR_NOT_DIVISIBLE = -2,     /* a length not divisible by a degree that must divide it */
+  CP_ERR_UNSUPPORTED_COMBO = -3, /* a flag combination the requirements table rules out */
+  CP_ERR_ALIGNMENT = -4,         /* a pointer or stride breaks the 16-byte rule */
+  CP_ERR_CUDA = -5,              /* a CUDA launch or runtime call failed */
+  CP_ERR_TIMEOUT = -6,           /* a kernel's bounded device wait expired */
+  CP_ERR_WORKSPACE = -7,         /* workspace missing or smaller than cp_attention_workspace_size */
+  CP_ERR_UNSUPPORTED_DEVICE = -8 /* the current device is not sm_103 */
+} cp_status;
+
+typedef enum { CP_BF16 = 0, CP_F32 = 1 } cp_dtype;
+
+/* How cp_attention_fwd runs the ring lap (both give full attention):
+ *   CP_LAP_FUSED    one kernel launch; every Q tile walks the K/V blocks in
+ *                   ring order (own block first, then its predecessor's, ...)
+ *                   and the per-block (out, lse) merge is the running online
+ *                   softmax state kept on chip.
+ *   CP_LAP_STEPWISE one block-attention launch per ring step over all ranks,
+ *                   each writing its fp32 (out, lse) partial, followed by an
+ *                   cp_lse_merge launch into the accumulator (steps >= 1). */
+typedef enum { CP_LAP_FUSED = 0, CP_LAP_STEPWISE = 1 } cp_lap_mode;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* cp_status_string(cp_status s);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int cp_version(void);
+
+/*
+ * Block attention of one query shard against one K/V block ("each device
+ * computes attention between its local Q and the KV block it holds": the
+ * "Paralelismo" API page, ContextParallelConfig.ring_degree; fp32 output and
+ * LSE: ContextParallelConfig.convert_to_fp32).
+ *   q    [B, Sq, H, D] (dt), batch stride q_bstride elements (0 = Sq*H*D)
+ *   k, v [B, Skv, H, D] (dt), batch stride kv_bstride elements (0 = Skv*H*D)
+ *   out  [B, Sq, H, D] float32, batch stride o_bstride elements (0 = Sq*H*D)
+ *   lse  [B, H, Sq] float32, dense
+ *   out[b,i,h,:] = sum_j softmax_j(scale * q[b,i,h,:].k[b,j,h,:]) v[b,j,h,:]
+ *   lse[b,h,i]   = ln sum_j exp(scale * q[b,i,h,:].k[b,j,h,:])
+ * Skv == 0 is allowed and yields out = 0, lse = -inf (the merge identity).
+ * Sq == 0 or B == 0 launches nothing. Errors: INVALID_ARG, ALIGNMENT, CUDA,
+ * UNSUPPORTED_DEVICE.
+ */
+cp_status cp_block_attn_fwd(const void* q, const void* k, const void* v, float* out, float* lse,
+                            int B, int H, int Sq, int Skv, int D, float scale,
+                            int64_t q_bstride, int64_t kv_bstride, int64_t o_bstride,
+                            cp_dtype dt, void* stream);
+
+/*
+ * In-place fp32 LSE merge of a block partial into an accumulator (the step
+ * that combines ring partials; "Paralelismo" API page, convert_to_fp32).
+ *   out_acc, out_blk [B, S, H, D] float32 dense; lse_acc, lse_blk [B, H, S]
+ *   m = max(lse_acc, lse_blk); lse = m + ln(e^(lse_acc-m) + e^(lse_blk-m))
+ *   out_acc = e^(lse_acc-lse) out_acc + e^(lse_blk-lse) out_blk; lse_acc = lse
+ * Rows where both LSEs are -inf become (0, -inf); merging with (0, -inf)
+ * returns the other operand. out_blk/lse_blk must not alias the accumulator.
+ * D must be a multiple of 4. Errors: INVALID_ARG, ALIGNMENT, CUDA.
+ */
+cp_status cp_lse_merge(float* out_acc, float* lse_acc, const float* out_blk, const float* lse_blk,
+                       int B, int H, int S, int D, void* stream);
+
+/*
+ * Ulysses all-to-all #1, sequence-sharded -> head-sharded ("Atenção Ulysses":
+ * the first all-to-all regroups so that each GPU holds every token of a subset
+ * of heads). Head group g is heads [g*H/U, (g+1)*H/U); tokens are concatenated
+ * in rank order:
+ *   in  [U][B, S/U, H, D]   (rank u's sequence shard, ranks stacked)
+ *   out [U][B, S, H/U, D]   (group g's heads, groups stacked)
+ *   out[g][b, u*S/U + s, h, d] = in[u][b, s, g*H/U + h, d]
+ * elem_bytes is the element size (2 for bf16, 4 for f32); a pure byte copy,
+ * bit-exact. Errors: INVALID_ARG (H or S not divisible by U, U > H),
+ * ALIGNMENT, CUDA.
+ */
+cp_status cp_ulysses_seq2head(const void* in, void* out, int U, int B, int S, int H, int D,
+                              int elem_bytes, void* stream);
+
+/*
+ * Ulysses all-to-all #2, the inverse of cp_ulysses_seq2head ("a second
+ * all-to-all regroups the results by token"):
+ *   in  [U][B, S, H/U, D] -> out [U][B, S/U, H, D]
+ *   out[u][b, s, g*H/U + h, d] = in[g][b, u*S/U + s, h, d]
+ */
+cp_status cp_ulysses_head2seq(const void* in, void* out, int U, int B, int S, int H, int D,
+                              int elem_bytes, void* stream);
+
+/*
+ * Host-only: the status cp_attention_fwd would return for these sizes and
+ * flags before touching any pointer (the requirements table of the
+ * "Paralelismo de contexto" page):
+ *   ring needs S % ring_degree == 0 unless uneven_ok (Ring Anything);
+ *   Ulysses needs S and H divisible by ulysses_degree, ulysses_degree <= H;
+ *   unified (both > 1) needs S % (ring_degree*ulysses_degree) == 0;
+ *   uneven_ok needs ring_degree > 1 and ulysses_degree == 1.
+ * Checks, in order: sizes/D/dtype/degrees >= 1 (INVALID_ARG), the uneven_ok
+ * combination (UNSUPPORTED_COMBO), ulysses_degree > H (INVALID_ARG), then
+ * divisibility (NOT_DIVISIBLE).
+ */
+cp_status cp_attention_validate(int B, int H, int S, int D, int ring_degree, int ulysses_degree,
+                                int uneven_ok, cp_dtype dt);
+
+/*
+ * Host-only: the ring shard table ("Ring Anything Attention" pads each rank's
+ * K/V to the longest local length; the split itself is this library's
+ * reading): contiguous ranges, the first S mod n ranks get ceil(S/n) tokens
+ * and the rest floor(S/n). Writes n offsets and n lengths (host arrays).
+ * Returns NOT_DIVISIBLE when S % n != 0 and !uneven_ok.
+ */
+cp_status cp_ring_shard_table(int S, int n, int uneven_ok, int* offsets, int* lengths);
+
+/* Host-only: bytes of device workspace cp_attention_fwd needs (0 if none). */
+size_t cp_attention_workspace_size(int B, int H, int S, int D, int ring_degree, int ulysses_degree,
+                                   cp_dtype dt, cp_lap_mode mode);
+
+/* Host-only: how many kernels cp_attention_fwd launches for these arguments. */
+int cp_attention_launch_count(int B, int H, int S, int D, int ring_degree, int ulysses_degree,
+                              cp_dtype dt, cp_lap_mode mode);
+
+/*
+ * Context-parallel attention forward over the GLOBAL tensors, with the ranks
+ * simulated on this GPU (the variants of the "Paralelismo de contexto" page,
+ * configured as in ContextParallelConfig):
+ *   q, k, v [B, S, H, D] (dt, dense); out [B, S, H, D] float32; lse [B, H, S]
+ *   ulysses_degree == 1: ring lap over ring_degree ranks (ring_degree == 1 is
+ *     plain attention); with uneven_ok the shards follow cp_ring_shard_table
+ *     (Ring Anything);
+ *   ulysses_degree > 1, ring_degree == 1: seq2head of q, k, v into the
+ *     workspace, attention per head group over all S tokens, head2seq of out
+ *     and lse;
+ *   both > 1 (unified): the same regroups, with a ring lap of ring_degree
+ *     ranks over each head group's sequence (device (r, u) holds token chunk
+ *     r*ulysses_degree + u; ring row r holds tokens [r*S/R, (r+1)*S/R)).
+ * The result equals full attention. workspace must hold
+ * cp_attention_workspace_size(...) bytes (may be NULL when that is 0).
+ * Errors: those of cp_attention_validate, plus INVALID_ARG (null pointers),
+ * ALIGNMENT, WORKSPACE, CUDA, UNSUPPORTED_DEVICE.
+ */
+cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* out, float* lse,
+                           int B, int H, int S, int D, float scale,
+                           int ring_degree, int ulysses_degree, int uneven_ok,
+                           void* workspace, size_t ws_bytes, cp_dtype dt, cp_lap_mode mode,
+                           void* stream);
+
+/*
+ * Synchronizes stream, then reads and clears the device error word on the
+ * current device. Returns CP_OK if no kernel reported an expired wait since
+ * the last call, CP_ERR_TIMEOUT if one did, CP_ERR_CUDA if the read failed.
+ */
+cp_status cp_check_device_status(void* stream);
+
+/*
+ * Test hook for the bounded-wait machinery: launches one small kernel whose
+ * threads wait on a shared-memory barrier that nothing completes, through the
+ * same bounded wait the attention kernel uses, with a limit of timeout_us
+ * microseconds (1..1000000). The kernel then records CP_ERR_TIMEOUT in the
+ * device error word and returns; it never faults or hangs.
+ */
+cp_status cp_debug_bounded_wait_probe(int timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CP_ATTN_H_ */
