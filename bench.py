@@ -412,6 +412,8 @@ def run_ours(args, w, world, rank, local):
                 "gpu_launches": launches_per_step * args.steps,
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks.summary(),
                 "parity_sample": parity,
+                "device": {"name": torch.cuda.get_device_name(dev),
+                           "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
                 "step_ms_min": min(per_step_ms), "step_ms_median": statistics.median(per_step_ms)}
     return line
 

@@ -25,7 +25,9 @@
 //   warps 2-3     idle.
 //   warps 4-7     softmax of query tile 0, warps 8-11 of tile 1: one thread
 //                 per query row (TMEM lane), row max and sum in registers,
-//                 P = 2^(s*scale*log2e - m) rounded to bf16 into TMEM over S,
+//                 P = 2^(s*scale*log2e - m) rounded to bf16 into TMEM over S
+//                 (l sums the rounded P, so out and lse are exact attention of
+//                 logits perturbed by at most one bf16 rounding of P),
 //                 O rescaled in TMEM only when the row max grows by more than
 //                 2^8 (the stale maximum is exact: it cancels in O / l).
 //                 Epilogue: O / l staged through shared memory and stored
@@ -331,16 +333,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kTileN; ++c)
             if (c >= nv) sr[c] = __float_as_uint(-INFINITY);
         }
-        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+        float mx[4];
 #pragma unroll
-        for (int c = 4; c < kTileN; c += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-          mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+        for (int c = 0; c < 4; ++c) mx[c] = __uint_as_float(sr[c]);
+#pragma unroll
+        for (int c = 4; c < kTileN; c += 8) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            mx[u] = fmax3(mx[u], __uint_as_float(sr[c + u]), __uint_as_float(sr[c + 4 + u]));
         }
-        const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const float mxs = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
         const bool need = mxs > m_used + kRescaleThreshold;
         const bool warp_rescale = __any_sync(0xffffffffu, need);
         float f = 1.f;
@@ -358,9 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e) {
             const float p0 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e]), sl2, nm));
             const float p1 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e + 1]), sl2, nm));
-            ls[(2 * e) & 3] += p0;
-            ls[(2 * e + 1) & 3] += p1;
             pk[e] = pack_bf16x2(p0, p1);
+            // row sum of the bf16-rounded P that the PV product consumes, so
+            // that O / l is a convex combination of V rows
+            add_bf16x2_to_f32(ls[(2 * e) & 3], ls[(2 * e + 1) & 3], pk[e]);
           }
           tmem_st32(t_s + half * 32, pk);
         }

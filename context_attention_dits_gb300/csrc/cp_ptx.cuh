@@ -205,6 +205,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (three-input form, sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// s0 += low bf16 of pk, s1 += high bf16 of pk (mixed-precision adds, sm_100+).
+__device__ __forceinline__ void add_bf16x2_to_f32(float& s0, float& s1, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "r"(pk));
+}
+
 // Pack two floats to bf16x2 with round-to-nearest-even; `lo` lands in the low
 // half (the element with the smaller column index).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
