@@ -44,7 +44,9 @@ SIGNATURES = {
     "cp_attention_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz, _i, _i, _vp]),
     "cp_check_device_status": (_i, [_vp]),
     "cp_debug_bounded_wait_probe": (_i, [_i, _vp]),
+    "cp_attention_fwd_no_alloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _i, _i, _vp]),
 }
+CP_NO_ALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None

@@ -155,6 +155,28 @@ def cp_attention_fwd(q, k, v, out, lse, scale: float, ring_degree: int = 1, ulys
     check(st, "cp_attention_fwd")
 
 
+def cp_attention_fwd_no_alloc(q, k, v, out, lse, scale: float, ring_degree: int = 1, ulysses_degree: int = 1,
+                              uneven_ok: bool = False, mode="fused", stream=None):
+    """cp_attention_fwd with the library's built-in 64 MiB device workspace (no allocation).
+
+    For callers that cannot allocate device memory. All calls share the
+    built-in workspace: calls that overlap on the GPU race.
+    """
+    _cuda(q, k, v, out, lse)
+    B, S, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape or out.shape != q.shape or lse.shape != (B, H, S):
+        raise ValueError("shape mismatch")
+    if q.dtype != k.dtype or q.dtype != v.dtype or out.dtype != torch.float32 or lse.dtype != torch.float32:
+        raise TypeError("q, k, v must share a dtype; out and lse must be float32")
+    for t in (q, k, v, out, lse):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be dense")
+    st = lib().cp_attention_fwd_no_alloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                         B, H, S, D, float(scale), ring_degree, ulysses_degree, int(bool(uneven_ok)),
+                                         _dt(q), _mode(mode), _stream(stream))
+    check(st, "cp_attention_fwd_no_alloc")
+
+
 def cp_check_device_status(stream=None) -> int:
     """Synchronizes the stream; returns 0, or CP_ERR_TIMEOUT if a kernel's bounded wait expired."""
     return int(lib().cp_check_device_status(_stream(stream)))
@@ -175,5 +197,5 @@ def cp_version() -> int:
 __all__ = [
     "CpError", "cp_block_attn_fwd", "cp_lse_merge", "cp_ulysses_seq2head", "cp_ulysses_head2seq",
     "cp_attention_validate", "cp_ring_shard_table", "cp_attention_workspace_size", "cp_attention_launch_count",
-    "cp_attention_fwd", "cp_check_device_status", "cp_debug_bounded_wait_probe", "cp_status_string", "cp_version",
+    "cp_attention_fwd", "cp_attention_fwd_no_alloc", "cp_check_device_status", "cp_debug_bounded_wait_probe", "cp_status_string", "cp_version",
 ]

@@ -454,3 +454,49 @@ cp_status cp_debug_bounded_wait_probe(int timeout_us, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// cp_attention_fwd_no_alloc: the workspace is a static device array of this
+// file instead of caller memory. Host code sees only a stand-in for the
+// array's symbol, so its device address is looked up once per device (with
+// that device current) and handed to the kernels as the workspace pointer.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_no_alloc_ws[CP_NO_ALLOC_WORKSPACE_BYTES];
+
+void* g_no_alloc_ws_addr[kMaxDevices];
+std::mutex g_no_alloc_mu;
+
+cp_status no_alloc_workspace(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CP_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_no_alloc_mu);
+  if (!g_no_alloc_ws_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_no_alloc_ws) != cudaSuccess || !p) return CP_ERR_CUDA;
+    g_no_alloc_ws_addr[dev] = p;
+  }
+  *out = g_no_alloc_ws_addr[dev];
+  return CP_OK;
+}
+
+}  // namespace
+
+extern "C" cp_status cp_attention_fwd_no_alloc(const void* q, const void* k, const void* v, float* out, float* lse,
+                                               int B, int H, int S, int D, float scale, int ring_degree,
+                                               int ulysses_degree, int uneven_ok, cp_dtype dt, cp_lap_mode mode,
+                                               void* stream) {
+  cp_status st = cp_attention_validate(B, H, S, D, ring_degree, ulysses_degree, uneven_ok, dt);
+  if (st != CP_OK) return st;
+  if (mode != CP_LAP_FUSED && mode != CP_LAP_STEPWISE) return CP_ERR_INVALID_ARG;
+  const size_t need = cp_attention_workspace_size(B, H, S, D, ring_degree, ulysses_degree, dt, mode);
+  if (need > CP_NO_ALLOC_WORKSPACE_BYTES) return CP_ERR_WORKSPACE;
+  if (B == 0 || S == 0) return CP_OK;
+  DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev)) != CP_OK) return st;
+  void* ws = nullptr;
+  if ((st = no_alloc_workspace(&ws)) != CP_OK) return st;
+  return cp_attention_fwd(q, k, v, out, lse, B, H, S, D, scale, ring_degree, ulysses_degree, uneven_ok, ws,
+                          CP_NO_ALLOC_WORKSPACE_BYTES, dt, mode, stream);
+}

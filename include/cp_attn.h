@@ -203,6 +203,32 @@ cp_status cp_check_device_status(void* stream);
  */
 cp_status cp_debug_bounded_wait_probe(int timeout_us, void* stream);
 
+/*
+ * cp_attention_fwd for callers that cannot allocate device memory. The pages
+ * have no counterpart to this call; it exists for integrations where device
+ * memory belongs to a host framework that gives a plugin no way to allocate,
+ * or where the latency and implicit synchronisation of a device allocation in
+ * the middle of a step are not acceptable. It takes the same arguments as
+ * cp_attention_fwd minus the workspace, and uses instead a workspace of
+ * CP_NO_ALLOC_WORKSPACE_BYTES (64 MiB) that the library holds as a static
+ * device array: every GPU that loads the library keeps those 64 MiB until the
+ * process exits. The first call on a device looks the array's device address
+ * up (once per device, with that device current); make that first call
+ * before any stream capture. No part of the array needs to start at zero
+ * (every byte used is written before it is read), but all calls share it:
+ * calls whose work overlaps on the GPU (other streams, other host threads)
+ * race on it and must be serialised by the caller. The call allocates no
+ * memory. Returns CP_ERR_WORKSPACE, launching nothing, when
+ * cp_attention_workspace_size(...) for these arguments exceeds
+ * CP_NO_ALLOC_WORKSPACE_BYTES (e.g. Ulysses at 4608 tokens x 24 heads x 128
+ * needs ~141 MB); otherwise the errors of cp_attention_fwd.
+ */
+#define CP_NO_ALLOC_WORKSPACE_BYTES (64u * 1024u * 1024u)
+cp_status cp_attention_fwd_no_alloc(const void* q, const void* k, const void* v, float* out, float* lse,
+                                    int B, int H, int S, int D, float scale,
+                                    int ring_degree, int ulysses_degree, int uneven_ok,
+                                    cp_dtype dt, cp_lap_mode mode, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
