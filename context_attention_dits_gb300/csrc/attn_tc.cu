@@ -130,8 +130,8 @@ __device__ __forceinline__ int total_tiles(const RingGeom& g, int r) {
 // Bounded wait that ignores the abort flag (used while draining).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > timeout_ns) return;
+  for (uint32_t n = 1; !mbar_try_wait(bar, parity); ++n) {
+    if ((n & 255u) == 0 && global_timer_ns() - t0 > timeout_ns) return;
   }
 }
 
@@ -268,35 +268,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait_bounded(bar(kBarQFull), 0, abort_flag, a.err, tmo) &&
                 mbar_wait_bounded(bar(kBarKFull), 0, abort_flag, a.err, tmo);
       if (ok) {
-        tc_fence_after();
         for (int i = 0; i < nq; ++i) {
           issue_s(i, 0);
           mma_commit(bar(kBarSFull + i));
         }
         mma_commit(bar(kBarKEmpty));
       }
+      // The tensor pipe queues about one MMA: whatever this thread does
+      // between two MMA groups leaves the pipe idle. Each step therefore
+      // waits at two points only: V(it), K(it+1) and P_0(it) before
+      // PV_0(it) + S_0(it+1); P_1(it) before PV_1(it) + S_1(it+1).
       for (int it = 0; ok && it < NT; ++it) {
         const int s = it & 1;
         const uint32_t ph = (it >> 1) & 1;
-        if (!mbar_wait_bounded(bar(kBarVFull + s), ph, abort_flag, a.err, tmo)) { ok = false; break; }
+        const bool more = it + 1 < NT;
+        const int s2 = (it + 1) & 1;
+        if (!mbar_wait_bounded(bar(kBarVFull + s), ph, abort_flag, a.err, tmo) ||
+            (more && !mbar_wait_bounded(bar(kBarKFull + s2), ((it + 1) >> 1) & 1, abort_flag, a.err, tmo))) {
+          ok = false;
+          break;
+        }
         for (int i = 0; i < nq; ++i) {
           if (!mbar_wait_bounded(bar(kBarPFull + i), it & 1, abort_flag, a.err, tmo)) { ok = false; break; }
           tc_fence_after();
           issue_pv(i, s, it > 0);
+          if (more) issue_s(i, s2);
           if (it == NT - 1) mma_commit(bar(kBarOFull + i));
-          if (i == nq - 1) mma_commit(bar(kBarVEmpty + s));
-          if (it + 1 < NT) {
-            const int s2 = (it + 1) & 1;
-            if (i == 0) {
-              if (!mbar_wait_bounded(bar(kBarKFull + s2), ((it + 1) >> 1) & 1, abort_flag, a.err, tmo)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-            }
-            issue_s(i, s2);
-            mma_commit(bar(kBarSFull + i));
-            if (i == nq - 1) mma_commit(bar(kBarKEmpty + s2));
+          if (more) mma_commit(bar(kBarSFull + i));
+          if (i == nq - 1) {
+            mma_commit(bar(kBarVEmpty + s));
+            if (more) mma_commit(bar(kBarKEmpty + s2));
           }
         }
       }

@@ -57,17 +57,25 @@ enum : uint32_t { kDevErrTimeout = 1u };
 // Returns true on completion. Returns false when another role of the CTA has
 // already aborted (*abort != 0) or when timeout_ns elapses; in the latter case
 // this thread raises the abort flag and records kDevErrTimeout in *err.
+// The abort flag and the global timer are consulted only every 256 polls:
+// reading them on every poll slows the loop's reaction to the barrier's
+// completion by hundreds of cycles.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
                                                   uint32_t* err, uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > timeout_ns) {
-      *abort = 1u;
-      atomicOr(err, kDevErrTimeout);
-      return false;
+    if ((n & 255u) == 0) {
+      if (*abort) return false;
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > timeout_ns) {
+        *abort = 1u;
+        atomicOr(err, kDevErrTimeout);
+        return false;
+      }
     }
   }
 }
