@@ -247,23 +247,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && NT > 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kTileM, kTileN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kTileM, D, false, true);
+      // Descriptor halves of every operand buffer, built once (see
+      // mma_ss_lohi: nothing but an add may sit between two MMAs).
+      const uint64_t dq = smem_desc_sw128(sb + L::kOffQ, 16, 1024);
+      const uint64_t dk = smem_desc_sw128(sb + L::kOffK, 16, 1024);
+      const uint64_t dv = smem_desc_sw128(sb + L::kOffV, L::kHalf, 1024);
+      const uint32_t qk_hi = static_cast<uint32_t>(dq >> 32);  // same for Q and K (SBO 1024, 128B swizzle)
+      const uint32_t v_hi = static_cast<uint32_t>(dv >> 32);
+      const uint32_t q_lo = static_cast<uint32_t>(dq), k_lo = static_cast<uint32_t>(dk);
+      const uint32_t v_lo = static_cast<uint32_t>(dv);
       auto issue_s = [&](int i, int stage) {
-        const uint32_t qa = sb + L::kOffQ + i * L::kQTile;
-        const uint32_t ka = sb + L::kOffK + stage * L::kKVTile;
+        const uint32_t a0 = q_lo + ((i * L::kQTile) >> 4);
+        const uint32_t b0 = k_lo + ((stage * L::kKVTile) >> 4);
+        const uint32_t d_tmem = tmem + i * kTileN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kHalf + (kk & 3) * 32;
-          mma_ss(tmem + i * kTileN, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4;
+          mma_ss_lohi(d_tmem, a0 + off, qk_hi, b0 + off, qk_hi, idesc_s, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int i, int stage, bool acc) {
-        const uint32_t va = sb + L::kOffV + stage * L::kKVTile;
+        const uint32_t b0 = v_lo + ((stage * L::kKVTile) >> 4);
+        const uint32_t d_tmem = tmem + 256 + i * D;
+        const uint32_t a_tmem = tmem + i * kTileN;
+        const uint32_t acc0 = acc ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          mma_ts(tmem + 256 + i * D, tmem + i * kTileN + kk * 8, smem_desc_sw128(va + kk * 2048, L::kHalf, 1024),
-                 idesc_o, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          mma_ts_lohi(d_tmem, a_tmem + kk * 8, b0 + ((kk * 2048) >> 4), v_hi, idesc_o, kk > 0 ? 1u : acc0);
       };
       bool ok = mbar_wait_bounded(bar(kBarQFull), 0, abort_flag, a.err, tmo) &&
                 mbar_wait_bounded(bar(kBarKFull), 0, abort_flag, a.err, tmo);
