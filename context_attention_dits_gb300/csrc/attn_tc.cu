@@ -344,16 +344,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kTileN; ++c)
             if (c >= nv) sr[c] = __float_as_uint(-INFINITY);
         }
-        float mx[4];
+        float mx[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) mx[c] = __uint_as_float(sr[c]);
+        for (int c = 0; c < 8; ++c) mx[c] = fmaxf(__uint_as_float(sr[c]), __uint_as_float(sr[8 + c]));
 #pragma unroll
-        for (int c = 4; c < kTileN; c += 8) {
+        for (int c = 16; c < kTileN; c += 16) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            mx[u] = fmax3(mx[u], __uint_as_float(sr[c + u]), __uint_as_float(sr[c + 4 + u]));
+          for (int u = 0; u < 8; ++u)
+            mx[u] = fmax3(mx[u], __uint_as_float(sr[c + u]), __uint_as_float(sr[c + 8 + u]));
         }
-        const float mxs = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        const float mxs =
+            fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
         const bool need = mxs > m_used + kRescaleThreshold;
         const bool warp_rescale = __any_sync(0xffffffffu, need);
         float f = 1.f;
