@@ -42,6 +42,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "cp_internal.h"
 #include "cp_ptx.cuh"
@@ -287,30 +288,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The tensor pipe queues about one MMA: whatever this thread does
       // between two MMA groups leaves the pipe idle. Each step therefore
       // waits at two points only: V(it), K(it+1) and P_0(it) before
-      // PV_0(it) + S_0(it+1); P_1(it) before PV_1(it) + S_1(it+1).
-      for (int it = 0; ok && it < NT; ++it) {
-        const int s = it & 1;
+      // PV_0(it) + S_0(it+1); P_1(it) before PV_1(it) + S_1(it+1). The step
+      // is instantiated per tile count and ring stage so that every MMA
+      // operand is a compile-time offset from one base: a run-time tile or
+      // stage index in the issue sequence measurably stalls the pipe.
+      auto step = [&](auto nq_c, auto stage_c, int it) -> bool {
+        constexpr int kNq = decltype(nq_c)::value;
+        constexpr int s = decltype(stage_c)::value;
+        constexpr int s2 = s ^ 1;
         const uint32_t ph = (it >> 1) & 1;
         const bool more = it + 1 < NT;
-        const int s2 = (it + 1) & 1;
         if (!mbar_wait_bounded(bar(kBarVFull + s), ph, abort_flag, a.err, tmo) ||
-            (more && !mbar_wait_bounded(bar(kBarKFull + s2), ((it + 1) >> 1) & 1, abort_flag, a.err, tmo))) {
-          ok = false;
-          break;
-        }
-        for (int i = 0; i < nq; ++i) {
-          if (!mbar_wait_bounded(bar(kBarPFull + i), it & 1, abort_flag, a.err, tmo)) { ok = false; break; }
+            (more && !mbar_wait_bounded(bar(kBarKFull + s2), ((it + 1) >> 1) & 1, abort_flag, a.err, tmo)))
+          return false;
+#pragma unroll
+        for (int i = 0; i < kNq; ++i) {
+          if (!mbar_wait_bounded(bar(kBarPFull + i), it & 1, abort_flag, a.err, tmo)) return false;
           tc_fence_after();
           issue_pv(i, s, it > 0);
-          if (more) issue_s(i, s2);
-          if (it == NT - 1) mma_commit(bar(kBarOFull + i));
-          if (more) mma_commit(bar(kBarSFull + i));
-          if (i == nq - 1) {
+          if (more) {
+            issue_s(i, s2);
+            mma_commit(bar(kBarSFull + i));
+          } else {
+            mma_commit(bar(kBarOFull + i));
+          }
+          if (i == kNq - 1) {
             mma_commit(bar(kBarVEmpty + s));
             if (more) mma_commit(bar(kBarKEmpty + s2));
           }
         }
-      }
+        return true;
+      };
+      auto run_steps = [&](auto nq_c) {
+        for (int it = 0; ok && it < NT; it += 2) {
+          ok = step(nq_c, std::integral_constant<int, 0>{}, it);
+          if (ok && it + 1 < NT) ok = step(nq_c, std::integral_constant<int, 1>{}, it + 1);
+        }
+      };
+      if (nq == 2)
+        run_steps(std::integral_constant<int, 2>{});
+      else
+        run_steps(std::integral_constant<int, 1>{});
       if (!ok) {
         mma_commit(bar(kBarDrain));
         drain_wait(bar(kBarDrain), 0, tmo);
