@@ -14,7 +14,7 @@
 // GPU attends to the K/V block it holds, then passes it on; the "Paralelismo"
 // API page, ContextParallelConfig.convert_to_fp32: fp32 output and LSE.)
 //
-// Warp roles (384 threads):
+// Warp roles (320 threads):
 //   warp 0        TMA producer: Q tiles once, then K and V tiles through a
 //                 two-stage ring each, 128B-swizzled.
 //   warp 1        TMEM allocator and MMA issuer (one thread):
@@ -22,8 +22,8 @@
 //                 O_i += P_i V (TS MMA, P read from TMEM), ping-ponging the
 //                 two query tiles so that one tile's softmax overlaps the
 //                 other tile's MMAs.
-//   warps 2-3     idle.
-//   warps 4-7     softmax of query tile 0, warps 8-11 of tile 1: one thread
+//   warps 2-5     softmax of query tile 0, warps 6-9 of tile 1 (a warp reads
+//                 the TMEM lane quadrant warp id mod 4): one thread
 //                 per query row (TMEM lane), row max and sum in registers,
 //                 P = 2^(s*scale*log2e - m) rounded to bf16 into TMEM over S
 //                 (l sums the rounded P, so out and lse are exact attention of
@@ -53,7 +53,7 @@ __device__ uint32_t g_dev_error;  // the device error word (see cp_check_device_
 
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 2^8
 constexpr uint32_t kTmemCols = 512;
 
@@ -334,10 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(bar(kBarDrain), 0, tmo);
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 2) {
     // ===================== softmax + epilogue =====================
-    const int i = (warp - 4) >> 2;  // query tile of this warpgroup
-    const int wq = warp & 3;        // TMEM lane quadrant of this warp
+    const int i = (warp - 2) >> 2;  // query tile of this warpgroup
+    const int wq = warp & 3;        // TMEM lane quadrant of this warp (warp id mod 4)
     const int row = wq * 32 + lane;
     if (i < nq) {
       const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
