@@ -151,37 +151,60 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sb + L::kOffBar + 8 * i; };
   int blk_h, blk_b;
 
-  // ---- work item: all (tile pair, head, batch) items first, then all
-  // (single tile, head, batch) items; items vary fastest, then heads ----
+  // ---- work item: all two-tile items of all (head, batch) first, then all
+  // one-tile items; items vary fastest, then heads. A shard with an odd tile
+  // count leaves its last tile over. Over a whole ring lap every shard visits
+  // every K/V block, so two such leftover tiles of different shards share one
+  // item (and one K/V stream, in the first shard's ring order); only an odd
+  // one out, or any leftover of a single-step launch, runs alone. ----
   const int n_pairs = a.g.pair_prefix[a.g.n_q];
   const int n_single = a.g.single_prefix[a.g.n_q];
+  const int n_cross = a.g.step < 0 ? n_single / 2 : 0;
+  const int n_two = n_pairs + n_cross;
+  const int n_one = n_single - 2 * n_cross;
+  // shard holding leftover tile k, and the first row of that tile
+  auto leftover = [&](int k, int& shard, int& row0) {
+    int rr = 0;
+    while (rr + 1 < a.g.n_q && a.g.single_prefix[rr + 1] <= k) ++rr;
+    shard = rr;
+    row0 = a.g.q_off[rr] + (a.g.pair_prefix[rr + 1] - a.g.pair_prefix[rr]) * 2 * kTileM;
+  };
   int id = blockIdx.x;
-  int r = 0, qrow0, nq, rows0, rows1;
+  int r = 0, nq, qrow[2], rows[2];
   {
-    const int per_hb_pairs = n_pairs;
-    const int64_t pair_ctas = static_cast<int64_t>(n_pairs) * a.H * a.B;
+    const int64_t two_ctas = static_cast<int64_t>(n_two) * a.H * a.B;
     int item, h_, b_;
-    if (id < pair_ctas) {
-      item = id % per_hb_pairs;
-      h_ = (id / per_hb_pairs) % a.H;
-      b_ = id / (per_hb_pairs * a.H);
-      while (r + 1 < a.g.n_q && a.g.pair_prefix[r + 1] <= item) ++r;
-      const int lp = item - a.g.pair_prefix[r];
-      qrow0 = a.g.q_off[r] + lp * 2 * kTileM;
+    if (id < two_ctas) {
+      item = id % n_two;
+      h_ = (id / n_two) % a.H;
+      b_ = id / (n_two * a.H);
       nq = 2;
+      if (item < n_pairs) {
+        while (r + 1 < a.g.n_q && a.g.pair_prefix[r + 1] <= item) ++r;
+        qrow[0] = a.g.q_off[r] + (item - a.g.pair_prefix[r]) * 2 * kTileM;
+        qrow[1] = qrow[0] + kTileM;
+        const int rem = a.g.q_off[r] + a.g.q_len[r] - qrow[0];
+        rows[0] = min(kTileM, rem);
+        rows[1] = min(kTileM, rem - kTileM);
+      } else {
+        const int k = 2 * (item - n_pairs);
+        int r1;
+        leftover(k, r, qrow[0]);
+        leftover(k + 1, r1, qrow[1]);
+        rows[0] = a.g.q_off[r] + a.g.q_len[r] - qrow[0];
+        rows[1] = a.g.q_off[r1] + a.g.q_len[r1] - qrow[1];
+      }
     } else {
-      id -= static_cast<int>(pair_ctas);
-      item = id % n_single;
-      h_ = (id / n_single) % a.H;
-      b_ = id / (n_single * a.H);
-      while (r + 1 < a.g.n_q && a.g.single_prefix[r + 1] <= item) ++r;
-      // the single tile is the last tile of shard r
-      qrow0 = a.g.q_off[r] + (a.g.pair_prefix[r + 1] - a.g.pair_prefix[r]) * 2 * kTileM;
+      id -= static_cast<int>(two_ctas);
+      item = id % n_one;
+      h_ = (id / n_one) % a.H;
+      b_ = id / (n_one * a.H);
       nq = 1;
+      leftover(2 * n_cross + item, r, qrow[0]);
+      qrow[1] = qrow[0];
+      rows[0] = a.g.q_off[r] + a.g.q_len[r] - qrow[0];
+      rows[1] = 0;
     }
-    const int rem = a.g.q_off[r] + a.g.q_len[r] - qrow0;
-    rows0 = min(kTileM, rem);
-    rows1 = nq == 2 ? min(kTileM, rem - kTileM) : 0;
     blk_h = h_;
     blk_b = b_;
   }
@@ -214,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < nq; ++i)
         for (int c = 0; c < D / 64; ++c)
           tma_load_4d(sb + L::kOffQ + i * L::kQTile + c * L::kHalf, &tq, bar(kBarQFull), c * 64, h,
-                      qrow0 + i * kTileM, b);
+                      qrow[i], b);
       KvCursor cur;
       cur.init(a.g, r);
       for (int it = 0; it < NT; ++it) {
@@ -420,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && NT > 0) ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarOFull + i), 0, abort_flag, a.err, tmo));
       if (ok) {
         tc_fence_after();
-        const int rows_valid = i == 0 ? rows0 : rows1;
-        const int tok0 = qrow0 + i * kTileM;  // first token of this tile
+        const int rows_valid = rows[i];
+        const int tok0 = qrow[i];  // first token of this tile
         const float inv_l = NT > 0 ? 1.f / l : 0.f;
         const float lse_v = NT > 0 ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
         if (row < rows_valid) a.lse[b * a.l_bstride + h * a.l_hstride + tok0 + row] = lse_v;
@@ -494,7 +517,11 @@ cudaError_t launch_tc_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensor
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  const int64_t items = static_cast<int64_t>(a.g.pair_prefix[a.g.n_q] + a.g.single_prefix[a.g.n_q]) * a.H * a.B;
+  // two-tile items (pairs, plus leftover tiles paired across shards over a
+  // whole lap) and one-tile items; see the work-item decode in the kernel
+  const int n_single = a.g.single_prefix[a.g.n_q];
+  const int n_cross = a.g.step < 0 ? n_single / 2 : 0;
+  const int64_t items = static_cast<int64_t>(a.g.pair_prefix[a.g.n_q] + n_single - n_cross) * a.H * a.B;
   if (items == 0) return cudaSuccess;
   if (items > 0x7fffffff) return cudaErrorInvalidValue;
   attn_fwd_tc_kernel<D><<<dim3(static_cast<unsigned>(items)), kThreads, L::kAlloc, s>>>(tq, tk, tv, a);
