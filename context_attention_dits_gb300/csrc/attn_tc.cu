@@ -411,8 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e]), sl2, nm));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e + 1]), sl2, nm));
+            float x0, x1;
+            fma_f32x2(x0, x1, __uint_as_float(sr[half * 64 + 2 * e]), __uint_as_float(sr[half * 64 + 2 * e + 1]),
+                      sl2, nm);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
             pk[e] = pack_bf16x2(p0, p1);
             // row sum of the bf16-rounded P that the PV product consumes, so
             // that O / l is a convex combination of V rows

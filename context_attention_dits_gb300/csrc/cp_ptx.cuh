@@ -247,6 +247,16 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// (d0, d1) = (a0 * b + c, a1 * b + c) in one packed fp32x2 FMA (sm_100+):
+// half the issue slots of two scalar FMAs, same rounding.
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
 // s0 += low bf16 of pk, s1 += high bf16 of pk (mixed-precision adds, sm_100+).
 __device__ __forceinline__ void add_bf16x2_to_f32(float& s0, float& s1, uint32_t pk) {
   asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
