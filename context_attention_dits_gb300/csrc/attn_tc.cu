@@ -385,58 +385,85 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kTileN; ++c)
             if (c >= nv) sr[c] = __float_as_uint(-INFINITY);
         }
-        float mx[8];
+        // P = 2^(s*scale*log2e - m_used) rounded to bf16, packed in pairs into
+        // pk; returns the row sum of the rounded P (the values the PV product
+        // consumes, so that O / l is a convex combination of V rows). S stays
+        // intact in TMEM until P is stored over its first 64 columns.
+        uint32_t pk[kTileN / 2];
+        auto exp_pass = [&](float nm) -> float {
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 8; ++c) mx[c] = fmaxf(__uint_as_float(sr[c]), __uint_as_float(sr[8 + c]));
-#pragma unroll
-        for (int c = 16; c < kTileN; c += 16) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            mx[u] = fmax3(mx[u], __uint_as_float(sr[c + u]), __uint_as_float(sr[c + 8 + u]));
-        }
-        const float mxs =
-            fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
-        const bool need = mxs > m_used + kRescaleThreshold;
-        const bool warp_rescale = __any_sync(0xffffffffu, need);
-        float f = 1.f;
-        if (need) {
-          f = ex2_approx(m_used - mxs);  // 0 on the first tile (m_used = -inf)
-          m_used = mxs;
-        }
-        // P = 2^(s*scale*log2e - m_used), bf16, over the first 64 columns of S
-        const float nm = -m_used;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
+          for (int e = 0; e < kTileN / 2; ++e) {
             float x0, x1;
-            fma_f32x2(x0, x1, __uint_as_float(sr[half * 64 + 2 * e]), __uint_as_float(sr[half * 64 + 2 * e + 1]),
-                      sl2, nm);
-            const float p0 = ex2_approx(x0);
-            const float p1 = ex2_approx(x1);
-            pk[e] = pack_bf16x2(p0, p1);
-            // row sum of the bf16-rounded P that the PV product consumes, so
-            // that O / l is a convex combination of V rows
+            fma_f32x2(x0, x1, __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]), sl2, nm);
+            pk[e] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
             add_bf16x2_to_f32(ls[(2 * e) & 3], ls[(2 * e + 1) & 3], pk[e]);
           }
-          tmem_st32(t_s + half * 32, pk);
-        }
-        l = l * f + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-        // O is idle here: PV of the previous tile completed before S of this
-        // tile was committed, and PV of this tile waits for P.
-        if (warp_rescale && it > 0) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(t_o + c * 32, o);
-            tmem_wait_ld();
+          return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        };
+        auto row_max = [&]() -> float {  // of the raw scores, times scale*log2e
+          float mx[8];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-            tmem_st32(t_o + c * 32, o);
+          for (int c = 0; c < 8; ++c) mx[c] = fmaxf(__uint_as_float(sr[c]), __uint_as_float(sr[8 + c]));
+#pragma unroll
+          for (int c = 16; c < kTileN; c += 16) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              mx[u] = fmax3(mx[u], __uint_as_float(sr[c + u]), __uint_as_float(sr[c + 8 + u]));
+          }
+          return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
+        };
+        auto reload_s = [&]() {
+#pragma unroll
+          for (int c = 0; c < kTileN / 32; ++c)
+            tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+          tmem_wait_ld();
+          if (nv < kTileN) {
+#pragma unroll
+            for (int c = 0; c < kTileN; ++c)
+              if (c >= nv) sr[c] = __float_as_uint(-INFINITY);
+          }
+        };
+        float f = 1.f, lsum;
+        if (it == 0) {
+          // no running maximum yet: the row maximum first
+          m_used = row_max();
+          lsum = exp_pass(-m_used);
+        } else {
+          // speculatively with the running maximum. Every P is at most the
+          // row sum, so a row sum within 2^8 proves that the row maximum is
+          // within 2^8 of the running maximum (the bound the rescaling keeps;
+          // an overflow to inf fails the test too). Otherwise reload S, take
+          // the row maximum, move to it if it grew by more than 2^8, and redo
+          // the tile; O and l are rescaled by the same factor (O is idle
+          // here: PV of the previous tile completed before S of this tile was
+          // committed, and PV of this tile waits for P).
+          lsum = exp_pass(-m_used);
+          if (__any_sync(0xffffffffu, !(lsum <= 256.f))) {
+            reload_s();
+            const float mxs = row_max();
+            const bool need = mxs > m_used + kRescaleThreshold;
+            if (need) {
+              f = ex2_approx(m_used - mxs);
+              m_used = mxs;
+            }
+            lsum = exp_pass(-m_used);
+            if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+              for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(t_o + c * 32, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                tmem_st32(t_o + c * 32, o);
+              }
+            }
           }
         }
+        tmem_st32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        l = l * f + lsum;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
