@@ -268,7 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ===================== MMA issuer =====================
-    if (lane == 0 && NT > 0) {
+    // The whole warp runs the loop (every operand is warp-uniform); one
+    // elected lane issues the MMAs and commits.
+    const bool leader = elect_one();
+    if (NT > 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kTileM, kTileN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kTileM, D, false, true);
       // Descriptor halves of every operand buffer, built once (see
@@ -280,6 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t v_hi = static_cast<uint32_t>(dv >> 32);
       const uint32_t q_lo = static_cast<uint32_t>(dq), k_lo = static_cast<uint32_t>(dk);
       const uint32_t v_lo = static_cast<uint32_t>(dv);
+      auto commit = [&](uint32_t bar_addr) {
+        if (leader) mma_commit(bar_addr);
+      };
       auto issue_s = [&](int i, int stage) {
         const uint32_t a0 = q_lo + ((i * L::kQTile) >> 4);
         const uint32_t b0 = k_lo + ((stage * L::kKVTile) >> 4);
@@ -287,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4;
-          mma_ss_lohi(d_tmem, a0 + off, qk_hi, b0 + off, qk_hi, idesc_s, kk > 0 ? 1u : 0u);
+          if (leader) mma_ss_lohi(d_tmem, a0 + off, qk_hi, b0 + off, qk_hi, idesc_s, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int i, int stage, bool acc) {
@@ -297,16 +303,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acc0 = acc ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ts_lohi(d_tmem, a_tmem + kk * 8, b0 + ((kk * 2048) >> 4), v_hi, idesc_o, kk > 0 ? 1u : acc0);
+          if (leader) mma_ts_lohi(d_tmem, a_tmem + kk * 8, b0 + ((kk * 2048) >> 4), v_hi, idesc_o, kk > 0 ? 1u : acc0);
       };
       bool ok = mbar_wait_bounded(bar(kBarQFull), 0, abort_flag, a.err, tmo) &&
                 mbar_wait_bounded(bar(kBarKFull), 0, abort_flag, a.err, tmo);
       if (ok) {
         for (int i = 0; i < nq; ++i) {
           issue_s(i, 0);
-          mma_commit(bar(kBarSFull + i));
+          commit(bar(kBarSFull + i));
         }
-        mma_commit(bar(kBarKEmpty));
+        commit(bar(kBarKEmpty));
       }
       // The tensor pipe queues about one MMA: whatever this thread does
       // between two MMA groups leaves the pipe idle. Each step therefore
@@ -331,13 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_pv(i, s, it > 0);
           if (more) {
             issue_s(i, s2);
-            mma_commit(bar(kBarSFull + i));
+            commit(bar(kBarSFull + i));
           } else {
-            mma_commit(bar(kBarOFull + i));
+            commit(bar(kBarOFull + i));
           }
           if (i == kNq - 1) {
-            mma_commit(bar(kBarVEmpty + s));
-            if (more) mma_commit(bar(kBarKEmpty + s2));
+            commit(bar(kBarVEmpty + s));
+            if (more) commit(bar(kBarKEmpty + s2));
           }
         }
         return true;
@@ -353,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         run_steps(std::integral_constant<int, 1>{});
       if (!ok) {
-        mma_commit(bar(kBarDrain));
+        commit(bar(kBarDrain));
         drain_wait(bar(kBarDrain), 0, tmo);
       }
     }

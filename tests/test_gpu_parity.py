@@ -273,6 +273,51 @@ def test_cp_attention_small_grid(B, H, S, D, R, U, ev, mode, dtype):
     check_attn(out, lse, ro, rl, BF16_TOL if dtype == "bf16" else F32_TOL, f"grid {B},{H},{S},{D},{R},{U},{ev}")
 
 
+# Score patterns for the three branches of the tensor-core softmax after the
+# first K/V tile: exponentials with the running maximum kept (row sum <= 2^8);
+# row sum above 2^8 with the maximum grown by less than 2^8 (reload, same
+# maximum); maximum grown by more than 2^8 (rescale), including growth large
+# enough that the first try overflows to inf. q = e_0 for every row and key j
+# has k_j = c_j e_0, so the scores are c_j * scale exactly; the tile steps of
+# c (in log2 units of the scaled score) are listed per case.
+RESCALE_CASES = {
+    "kept": [0.0, -1.0, 0.5, -3.0],
+    "sum_over_no_rescale": [0.0, 3.0, 3.0, 2.0],
+    "rescale": [0.0, 3.0, 20.0, 25.0],
+    "overflow_then_rescale": [0.0, 200.0, 150.0, 260.0],
+}
+
+
+@pytest.mark.parametrize("case", sorted(RESCALE_CASES))
+@pytest.mark.parametrize("mode", ["fused", "stepwise"])
+def test_softmax_rescale_branches(case, mode):
+    steps = RESCALE_CASES[case]
+    B, H, D = 1, 2, 128
+    S = 128 * len(steps) - 37  # ragged last tile
+    scale = D ** -0.5
+    g = torch.Generator().manual_seed(7)
+    # per key: the tile's level (log2 units) minus a spread inside the tile, so
+    # that every tile has its own maximum and a range of values below it
+    lvl = torch.tensor([steps[j // 128] for j in range(S)], dtype=torch.float64)
+    spread = torch.rand(S, generator=g, dtype=torch.float64) * 6.0
+    c = (lvl - spread) / (scale * np.log2(np.e))
+    q = torch.zeros(B, S, H, D)
+    q[..., 0] = 1.0
+    k = torch.zeros(B, S, H, D)
+    k[..., 0] = c.float()[None, :, None]
+    v = torch.randn(B, S, H, D, generator=g)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+
+    class W:
+        pass
+    w = W()
+    w.scale, w.ring_degree, w.ulysses_degree, w.uneven_ok = scale, 2, 1, True
+    ro, rl = oracle.cp_attention(q, k, v, scale, 2, 1, True)
+    out, lse = run_fwd(*dev(q, k, v), w, mode)
+    check_attn(out, lse, ro, rl, BF16_TOL, f"rescale/{case}/{mode}")
+    assert cpa().cp_check_device_status() == 0
+
+
 def test_cp_attention_modes_agree_and_deterministic():
     w = WORKLOADS["flux_ring4"]
     q, k, v = dev(*make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed))
