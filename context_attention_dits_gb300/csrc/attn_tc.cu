@@ -228,32 +228,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ===================== TMA producer =====================
-    if (lane == 0 && NT > 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
+    // The whole warp runs the loop; one elected lane issues the copies.
+    const bool leader = elect_one();
+    if (NT > 0) {
+      if (leader) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+      }
       int k_issued[2] = {0, 0}, v_issued[2] = {0, 0};
-      mbar_arrive_expect_tx(bar(kBarQFull), nq * L::kQTile);
-      for (int i = 0; i < nq; ++i)
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sb + L::kOffQ + i * L::kQTile + c * L::kHalf, &tq, bar(kBarQFull), c * 64, h,
-                      qrow[i], b);
+      if (leader) {
+        mbar_arrive_expect_tx(bar(kBarQFull), nq * L::kQTile);
+        for (int i = 0; i < nq; ++i)
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sb + L::kOffQ + i * L::kQTile + c * L::kHalf, &tq, bar(kBarQFull), c * 64, h,
+                        qrow[i], b);
+      }
       KvCursor cur;
       cur.init(a.g, r);
       for (int it = 0; it < NT; ++it) {
         const int s = it & 1;
         const uint32_t ph = (it >> 1) & 1;
         if (!mbar_wait_bounded(bar(kBarKEmpty + s), ph ^ 1, abort_flag, a.err, tmo)) break;
-        mbar_arrive_expect_tx(bar(kBarKFull + s), L::kKVTile);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sb + L::kOffK + s * L::kKVTile + c * L::kHalf, &tk, bar(kBarKFull + s), c * 64, h,
-                      cur.kv0(), b);
+        if (leader) {
+          mbar_arrive_expect_tx(bar(kBarKFull + s), L::kKVTile);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sb + L::kOffK + s * L::kKVTile + c * L::kHalf, &tk, bar(kBarKFull + s), c * 64, h,
+                        cur.kv0(), b);
+        }
         ++k_issued[s];
         if (!mbar_wait_bounded(bar(kBarVEmpty + s), ph ^ 1, abort_flag, a.err, tmo)) break;
-        mbar_arrive_expect_tx(bar(kBarVFull + s), L::kKVTile);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sb + L::kOffV + s * L::kKVTile + c * L::kHalf, &tv, bar(kBarVFull + s), c * 64, h,
-                      cur.kv0(), b);
+        if (leader) {
+          mbar_arrive_expect_tx(bar(kBarVFull + s), L::kKVTile);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sb + L::kOffV + s * L::kKVTile + c * L::kHalf, &tv, bar(kBarVFull + s), c * 64, h,
+                        cur.kv0(), b);
+        }
         ++v_issued[s];
         cur.advance(a.g, r);
       }
