@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--mode", default="fused", choices=["fused", "stepwise"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the per-kernel HBM measurements and the other workloads")
     return ap.parse_args()
 
 
@@ -124,10 +126,116 @@ def cpu_baseline(w, q, k, v, budget_s=12.0):
         s.run()
         reps += 1
         el = time.perf_counter() - t0
-        if el >= budget_s * 0.6 or reps >= 3:
+        if el >= budget_s * 0.8:
             break
     return {"value": s.flops * reps / el / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
             "sample": s.describe(), "seconds": round(el, 3)}
+
+
+# ---------------------------------------------------------------------------
+# secondary lines: the HBM-bound kernels and the other workloads
+# ---------------------------------------------------------------------------
+def _time_events(fn, flush, stream, reps):
+    """Mean CUDA-event time (ms) of fn over reps runs, L2 flushed before each (outside the events)."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+    for i in range(reps):
+        flush.fill_(float(i))
+        st[i].record(stream)
+        fn()
+        en[i].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in zip(st, en)) / reps
+
+
+def _time_batch(fns, flush, stream, rounds):
+    """CUDA-event time (ms) per launch of the launch list fns run back to back, rounds times, L2
+    flushed once before each round (outside the events). The operands of fns together exceed L2, so
+    every launch reads from HBM; back-to-back launches overlap their launch latency, as the
+    launches of a stepwise lap do."""
+    import torch
+    for f in fns:
+        f()
+    torch.cuda.synchronize()
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(rounds)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(rounds)]
+    for i in range(rounds):
+        flush.fill_(float(i))
+        st[i].record(stream)
+        for f in fns:
+            f()
+        en[i].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in zip(st, en)) / (rounds * len(fns))
+
+
+def secondary(cpa, dev, flush, stream, peaks):
+    """Achieved bandwidth of the merge and regroup kernels (algorithmic bytes / event time) and the
+    throughput of cp_attention_fwd on the other workloads."""
+    import torch
+    from synth import WORKLOADS, make_merge_operands, make_qkv
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    res = {}
+
+    def bw(name, nbytes, ms_single, ms_batch, note):
+        res[name] = {"bytes_per_launch": nbytes, "single_launch": {"ms": ms_single, "GB_s": nbytes / ms_single / 1e6,
+                                                                   "frac_of_hbm": nbytes / ms_single / 1e6 / hbm},
+                     "back_to_back": {"ms": ms_batch, "GB_s": nbytes / ms_batch / 1e6,
+                                      "frac_of_hbm": nbytes / ms_batch / 1e6 / hbm},
+                     "note": note}
+
+    # LSE merge of one FLUX ring-4 rank-step partial: [1,1152,24,128] fp32 + lse [1,24,1152];
+    # a stepwise lap runs 12 of them. Eight operand sets (342 MB) rotate through the batch.
+    B, S, H, D = 1, 1152, 24, 128
+    sets = [[t.to(dev) for t in make_merge_operands(B, H, S, D, seed=5 + i)] for i in range(8)]
+    nbytes = 12 * sets[0][0].numel() + 12 * sets[0][1].numel()
+    fns = [lambda o=o: cpa.cp_lse_merge(o[0], o[1], o[2], o[3], stream=stream) for o in sets]
+    bw("lse_merge_flux_ring4_step", nbytes, _time_events(fns[0], flush, stream, 30),
+       _time_batch(fns * 3, flush, stream, 5), "one rank-step merge; back_to_back: 24 merges over 8 operand sets")
+    del sets, fns
+
+    # Ulysses regroups of FLUX Ulysses-4: q, k, v (bf16) seq->head; out (fp32) head->seq
+    U, S, H, D = 4, 4608, 24, 128
+    xs = [torch.randn((U, 1, S // U, H, D), device=dev).to(torch.bfloat16) for _ in range(6)]
+    ys = [torch.empty((U, 1, S, H // U, D), device=dev, dtype=torch.bfloat16) for _ in range(6)]
+    nbytes = 2 * xs[0].numel() * 2
+    fns = [lambda x=x, y=y: cpa.cp_ulysses_seq2head(x, y, stream=stream) for x, y in zip(xs, ys)]
+    bw("seq2head_flux_ulysses4_bf16", nbytes, _time_events(fns[0], flush, stream, 30),
+       _time_batch(fns * 2, flush, stream, 5), "one tensor; back_to_back: 12 regroups over 6 tensor pairs")
+    del xs, ys, fns
+    xs = [torch.randn((U, 1, S, H // U, D), device=dev) for _ in range(3)]
+    ys = [torch.empty((U, 1, S // U, H, D), device=dev) for _ in range(3)]
+    nbytes = 2 * xs[0].numel() * 4
+    fns = [lambda x=x, y=y: cpa.cp_ulysses_head2seq(x, y, stream=stream) for x, y in zip(xs, ys)]
+    bw("head2seq_flux_ulysses4_f32", nbytes, _time_events(fns[0], flush, stream, 30),
+       _time_batch(fns * 4, flush, stream, 5), "the fp32 output; back_to_back: 12 regroups over 3 tensor pairs")
+    del xs, ys, fns
+
+    # cp_attention_fwd on the other workloads (fused lap), inputs resident
+    for name in ("flux_ulysses4", "ring_anything3", "video_unified"):
+        w = WORKLOADS[name]
+        q, k, v = (t.to(dev) for t in make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed, w.q_mult))
+        out = torch.empty((w.B, w.S, w.H, w.D), device=dev)
+        lse = torch.empty((w.B, w.H, w.S), device=dev)
+        wsb = cpa.cp_attention_workspace_size(w.B, w.H, w.S, w.D, w.ring_degree, w.ulysses_degree, q.dtype, "fused")
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+        ms = _time_events(lambda: cpa.cp_attention_fwd(q, k, v, out, lse, w.scale, w.ring_degree,
+                                                        w.ulysses_degree, w.uneven_ok, workspace=ws,
+                                                        mode="fused", stream=stream),
+                          flush, stream, 5 if name == "video_unified" else 20)
+        tf = w.flops / (ms * 1e-3) / 1e12
+        res[name] = {"TFLOP_s": tf, "ms": ms, "frac_of_bf16_peak": tf / bf16,
+                     "launches": cpa.cp_attention_launch_count(w.B, w.H, w.S, w.D, w.ring_degree,
+                                                               w.ulysses_degree, q.dtype, "fused")}
+        del q, k, v, out, lse, ws
+    if cpa.cp_check_device_status() != 0:
+        raise RuntimeError("device status after the secondary measurements")
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -402,6 +510,9 @@ def run_ours(args, w, world, rank, local):
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             cpu = cpu_baseline(w, q_h, k_h, v_h)
+        sec = None
+        if world == 1 and not args.no_secondary:
+            sec = secondary(cpa, dev, flush, stream, peaks)
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
@@ -414,7 +525,8 @@ def run_ours(args, w, world, rank, local):
                 "parity_sample": parity,
                 "device": {"name": torch.cuda.get_device_name(dev),
                            "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
-                "step_ms_min": min(per_step_ms), "step_ms_median": statistics.median(per_step_ms)}
+                "step_ms_min": min(per_step_ms), "step_ms_median": statistics.median(per_step_ms),
+                "secondary": sec}
     return line
 
 

@@ -70,94 +70,174 @@ __global__ void __launch_bounds__(32 * kF32RowsPerCta) attn_fwd_f32_kernel(const
 }
 
 // ----------------------------------------------------------------------------
-// LSE merge. One CTA = kMergeTok consecutive tokens of one batch entry, all H
-// heads: the (h, token) weights are computed once into shared memory, then
-// the contiguous [kMergeTok, H, D] slab of out rows is streamed as float4.
+// LSE merge. Grid: x over token chunks, y over (batch, head) pairs, so a
+// CTA's rows share b and h and no index needs a division. A group of g lanes
+// owns one (b, token, h) row of D/4 float4 (g = D/4 when that divides 32,
+// else 32 lanes looping over the row); a warp takes 32/g rows per slot and
+// kMergeRows slots per pass. The rows' out loads are issued first, then their
+// LSE loads, so a pass waits for one memory round trip. Each lane computes
+// its row's weights itself, and the first lane of the row writes the merged
+// LSE once every lane of the row has read the old one.
 // ----------------------------------------------------------------------------
-constexpr int kMergeTok = 8;
 constexpr int kMergeThreads = 256;
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeRows = 4;
 
-__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(float* __restrict__ out_acc, float* __restrict__ lse_acc,
-                                                                  const float* __restrict__ out_blk,
-                                                                  const float* __restrict__ lse_blk, int H, int S,
-                                                                  int D) {
-  extern __shared__ float wsm[];  // [2][H][kMergeTok]: weight of acc, weight of blk
-  const int b = blockIdx.y;
-  const int t0 = blockIdx.x * kMergeTok;
-  const int nt = min(kMergeTok, S - t0);
-  float* wa = wsm;
-  float* wb = wsm + H * kMergeTok;
-  for (int idx = threadIdx.x; idx < H * kMergeTok; idx += blockDim.x) {
-    const int hh = idx / kMergeTok, tt = idx % kMergeTok;
-    if (tt >= nt) continue;
-    const int64_t li = (static_cast<int64_t>(b) * H + hh) * S + t0 + tt;
-    const float la = lse_acc[li], lb = lse_blk[li];
-    const float m = fmaxf(la, lb);
-    float ea = 0.f, eb = 0.f, lse = -INFINITY;
-    if (m != -INFINITY) {
-      const float xa = expf(la - m), xb = expf(lb - m);
-      lse = m + logf(xa + xb);
-      ea = expf(la - lse);
-      eb = expf(lb - lse);
+struct MergeW {
+  float wa, wb, lse;
+};
+
+__device__ __forceinline__ MergeW merge_weights(float la, float lb) {
+  const float m = fmaxf(la, lb);
+  if (m == -INFINITY) return {0.f, 0.f, -INFINITY};  // both partials empty
+  const float xa = __expf(la - m), xb = __expf(lb - m);  // one of them is exactly 1
+  const float sum = xa + xb;
+  const float inv = __fdividef(1.f, sum);
+  return {xa * inv, xb * inv, m + __logf(sum)};
+}
+
+__device__ __forceinline__ float4 merge4(const MergeW& w, const float4& p, const float4& q) {
+  return make_float4(w.wa * p.x + w.wb * q.x, w.wa * p.y + w.wb * q.y, w.wa * p.z + w.wb * q.z,
+                     w.wa * p.w + w.wb * q.w);
+}
+
+// Idx: the index type, int when every float4 and LSE index fits (the host
+// checks). kOneVec: D/4 divides 32, so each lane holds one float4 of a row.
+template <typename Idx, bool kOneVec>
+__global__ void __launch_bounds__(kMergeThreads, 4) lse_merge_kernel(float* __restrict__ out_acc,
+                                                                     float* __restrict__ lse_acc,
+                                                                     const float* __restrict__ out_blk,
+                                                                     const float* __restrict__ lse_blk, int B, int H,
+                                                                     int S, int dv) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = (dv <= 32 && 32 % dv == 0) ? dv : 32;  // lanes per row
+  const int rpw = 32 / g;                               // rows per warp slot
+  const int sub = lane / g, j0 = lane - sub * g;
+  const int per_cta = kMergeWarps * kMergeRows * rpw;  // tokens per CTA and (b, h)
+  const int s0 = blockIdx.x * per_cta;
+  float4* oa = reinterpret_cast<float4*>(out_acc);
+  const float4* ob = reinterpret_cast<const float4*>(out_blk);
+  for (int bh = blockIdx.y; bh < B * H; bh += gridDim.y) {
+    const int b = bh / H, h = bh - b * H;
+    const Idx lse0 = static_cast<Idx>(bh) * S;
+    // float4 index of element (b, t, h, 0)
+    auto vbase = [&](int t) { return ((static_cast<Idx>(b) * S + t) * H + h) * dv; };
+    int tok[kMergeRows];
+#pragma unroll
+    for (int u = 0; u < kMergeRows; ++u) tok[u] = s0 + (u * kMergeWarps + warp) * rpw + sub;
+    if (kOneVec) {
+      float4 p[kMergeRows], q[kMergeRows];
+#pragma unroll
+      for (int u = 0; u < kMergeRows; ++u)
+        if (tok[u] < S) {
+          p[u] = oa[vbase(tok[u]) + j0];
+          q[u] = ob[vbase(tok[u]) + j0];
+        }
+      float la[kMergeRows], lb[kMergeRows];
+#pragma unroll
+      for (int u = 0; u < kMergeRows; ++u) {
+        la[u] = tok[u] < S ? lse_acc[lse0 + tok[u]] : -INFINITY;
+        lb[u] = tok[u] < S ? lse_blk[lse0 + tok[u]] : -INFINITY;
+      }
+      __syncwarp();  // every lane of a row has read its old LSE
+#pragma unroll
+      for (int u = 0; u < kMergeRows; ++u)
+        if (tok[u] < S) {
+          const MergeW w = merge_weights(la[u], lb[u]);
+          oa[vbase(tok[u]) + j0] = merge4(w, p[u], q[u]);
+          if (j0 == 0) lse_acc[lse0 + tok[u]] = w.lse;
+        }
+    } else {
+      MergeW w[kMergeRows];
+#pragma unroll
+      for (int u = 0; u < kMergeRows; ++u)
+        w[u] = merge_weights(tok[u] < S ? lse_acc[lse0 + tok[u]] : -INFINITY,
+                             tok[u] < S ? lse_blk[lse0 + tok[u]] : -INFINITY);
+#pragma unroll
+      for (int u = 0; u < kMergeRows; ++u)
+        if (tok[u] < S)
+          for (int j = j0; j < dv; j += g) oa[vbase(tok[u]) + j] = merge4(w[u], oa[vbase(tok[u]) + j],
+                                                                          ob[vbase(tok[u]) + j]);
+      __syncwarp();  // every lane of a row has read its old LSE
+      if (j0 == 0) {
+#pragma unroll
+        for (int u = 0; u < kMergeRows; ++u)
+          if (tok[u] < S) lse_acc[lse0 + tok[u]] = w[u].lse;
+      }
     }
-    wa[idx] = ea;
-    wb[idx] = eb;
-    lse_acc[li] = lse;
-  }
-  __syncthreads();
-  const int64_t base = (static_cast<int64_t>(b) * S + t0) * H * D;
-  const int nvec = nt * H * D / 4;
-  const int dv = D / 4;
-  float4* oa = reinterpret_cast<float4*>(out_acc + base);
-  const float4* ob = reinterpret_cast<const float4*>(out_blk + base);
-#pragma unroll 4
-  for (int v = threadIdx.x; v < nvec; v += kMergeThreads) {
-    const int rowi = v / dv;  // (token, head) row within the slab
-    const int tt = rowi / H, hh = rowi - tt * H;
-    const float x = wa[hh * kMergeTok + tt], y = wb[hh * kMergeTok + tt];
-    const float4 p = oa[v], q = ob[v];
-    float4 o;
-    o.x = x * p.x + y * q.x;
-    o.y = x * p.y + y * q.y;
-    o.z = x * p.z + y * q.z;
-    o.w = x * p.w + y * q.w;
-    oa[v] = o;
   }
 }
 
 // ----------------------------------------------------------------------------
-// Segment copy: warp w copies output segment w (grid-stride), reading the
-// input segment at the strided offset. VEC-byte vectors.
+// Segment copy: warp w copies a contiguous range of output segments, two at a
+// time, advancing the strided input offset with carries (one index
+// decomposition per warp); every lane issues up to kCopySegs x kCopyVec loads
+// before its stores. VEC-byte vectors.
 // ----------------------------------------------------------------------------
+constexpr int kCopySegs = 2;
+constexpr int kCopyVec = 4;
+
 template <typename V>
-__global__ void __launch_bounds__(256) segment_copy_kernel(const SegCopy c) {
+__global__ void __launch_bounds__(256) segment_copy_kernel(const SegCopy c, int64_t per_warp) {
   const int lane = threadIdx.x & 31;
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int64_t nseg = c.n0 * c.n1 * c.n2 * c.n3;
   const int64_t seg_bytes = c.seg_elems * c.elem_bytes;
   const int64_t nv = seg_bytes / static_cast<int64_t>(sizeof(V));
   const char* in = static_cast<const char*>(c.in);
   char* out = static_cast<char*>(c.out);
-  for (int64_t sg = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); sg < nseg; sg += warps) {
-    int64_t rest = sg;
-    const int64_t i3 = rest % c.n3;
-    rest /= c.n3;
-    const int64_t i2 = rest % c.n2;
-    rest /= c.n2;
-    const int64_t i1 = rest % c.n1;
-    const int64_t i0 = rest / c.n1;
-    const int64_t src_el = i0 * c.st0 + i1 * c.st1 + i2 * c.st2 + i3 * c.st3;
-    const V* src = reinterpret_cast<const V*>(in + src_el * c.elem_bytes);
-    V* dst = reinterpret_cast<V*>(out + sg * seg_bytes);
-    int64_t v = lane;
-    for (; v + 96 < nv; v += 128) {
-      const V x0 = src[v], x1 = src[v + 32], x2 = src[v + 64], x3 = src[v + 96];
-      dst[v] = x0;
-      dst[v + 32] = x1;
-      dst[v + 64] = x2;
-      dst[v + 96] = x3;
+  int64_t sg = (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * per_warp;
+  const int64_t end = sg + per_warp < nseg ? sg + per_warp : nseg;
+  if (sg >= end) return;
+  int64_t rest = sg;
+  int64_t i3 = rest % c.n3;
+  rest /= c.n3;
+  int64_t i2 = rest % c.n2;
+  rest /= c.n2;
+  int64_t i1 = rest % c.n1;
+  int64_t src_el = (rest / c.n1) * c.st0 + i1 * c.st1 + i2 * c.st2 + i3 * c.st3;
+  auto advance = [&]() {  // to the next segment in (i0, i1, i2, i3) order
+    src_el += c.st3;
+    if (++i3 == c.n3) {
+      i3 = 0;
+      src_el += c.st2 - c.n3 * c.st3;
+      if (++i2 == c.n2) {
+        i2 = 0;
+        src_el += c.st1 - c.n2 * c.st2;
+        if (++i1 == c.n1) {
+          i1 = 0;
+          src_el += c.st0 - c.n1 * c.st1;
+        }
+      }
     }
-    for (; v < nv; v += 32) dst[v] = src[v];
+  };
+  for (; sg < end; sg += kCopySegs) {
+    const V* src[kCopySegs];
+    V* dst[kCopySegs];
+    bool ok[kCopySegs];
+#pragma unroll
+    for (int k = 0; k < kCopySegs; ++k) {
+      ok[k] = sg + k < end;
+      src[k] = reinterpret_cast<const V*>(in + src_el * c.elem_bytes);
+      dst[k] = reinterpret_cast<V*>(out + (sg + k) * seg_bytes);
+      if (ok[k]) advance();
+    }
+    for (int64_t base = 0; base < nv; base += 32 * kCopyVec) {
+      V x[kCopySegs][kCopyVec];
+#pragma unroll
+      for (int k = 0; k < kCopySegs; ++k)
+#pragma unroll
+        for (int j = 0; j < kCopyVec; ++j) {
+          const int64_t v = base + lane + 32 * j;
+          if (ok[k] && v < nv) x[k][j] = src[k][v];
+        }
+#pragma unroll
+      for (int k = 0; k < kCopySegs; ++k)
+#pragma unroll
+        for (int j = 0; j < kCopyVec; ++j) {
+          const int64_t v = base + lane + 32 * j;
+          if (ok[k] && v < nv) dst[k][v] = x[k][j];
+        }
+    }
   }
 }
 
@@ -180,9 +260,18 @@ cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t s) {
 cudaError_t launch_lse_merge(float* out_acc, float* lse_acc, const float* out_blk, const float* lse_blk, int B, int H,
                              int S, int D, cudaStream_t s) {
   if (B == 0 || S == 0 || H == 0) return cudaSuccess;
-  const size_t smem = 2 * static_cast<size_t>(H) * kMergeTok * sizeof(float);
-  dim3 grid((S + kMergeTok - 1) / kMergeTok, B);
-  lse_merge_kernel<<<grid, kMergeThreads, smem, s>>>(out_acc, lse_acc, out_blk, lse_blk, H, S, D);
+  const int dv = D / 4;
+  const int g = (dv <= 32 && 32 % dv == 0) ? dv : 32;
+  const int per_cta = kMergeWarps * kMergeRows * (32 / g);
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  dim3 grid((S + per_cta - 1) / per_cta, static_cast<unsigned>(bh < 65535 ? bh : 65535));
+  const bool small = bh * S * dv < (1LL << 31);
+  if (g == dv && small)
+    lse_merge_kernel<int, true><<<grid, kMergeThreads, 0, s>>>(out_acc, lse_acc, out_blk, lse_blk, B, H, S, dv);
+  else if (g == dv)
+    lse_merge_kernel<int64_t, true><<<grid, kMergeThreads, 0, s>>>(out_acc, lse_acc, out_blk, lse_blk, B, H, S, dv);
+  else
+    lse_merge_kernel<int64_t, false><<<grid, kMergeThreads, 0, s>>>(out_acc, lse_acc, out_blk, lse_blk, B, H, S, dv);
   return cudaGetLastError();
 }
 
@@ -193,16 +282,25 @@ cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = (nseg + 7) / 8;                 // 8 warps per CTA, one segment each
-  const int blocks = static_cast<int>(want < sms * 8LL ? want : sms * 8LL);
   uint64_t align = static_cast<uint64_t>(seg_bytes) | reinterpret_cast<uintptr_t>(c.in) |
                    reinterpret_cast<uintptr_t>(c.out);
   for (int64_t st : {c.st0, c.st1, c.st2, c.st3}) align |= static_cast<uint64_t>(st * c.elem_bytes);
-  if (align % 16 == 0) segment_copy_kernel<uint4><<<blocks, 256, 0, s>>>(c);
-  else if (align % 8 == 0) segment_copy_kernel<uint2><<<blocks, 256, 0, s>>>(c);
-  else if (align % 4 == 0) segment_copy_kernel<uint32_t><<<blocks, 256, 0, s>>>(c);
-  else segment_copy_kernel<uint8_t><<<blocks, 256, 0, s>>>(c);
-  return cudaGetLastError();
+  auto launch = [&](auto kernel) {
+    int per_sm = 1;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+    // one resident wave of 8-warp CTAs, each warp a contiguous range of segments
+    const int64_t warps_cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1) * 8;
+    const int64_t warps_want = (nseg + kCopySegs - 1) / kCopySegs;
+    const int64_t warps = warps_want < warps_cap ? warps_want : warps_cap;
+    const int64_t per_warp = (nseg + warps - 1) / warps;
+    const int64_t blocks = ((nseg + per_warp - 1) / per_warp + 7) / 8;
+    kernel<<<static_cast<int>(blocks), 256, 0, s>>>(c, per_warp);
+    return cudaGetLastError();
+  };
+  if (align % 16 == 0) return launch(segment_copy_kernel<uint4>);
+  if (align % 8 == 0) return launch(segment_copy_kernel<uint2>);
+  if (align % 4 == 0) return launch(segment_copy_kernel<uint32_t>);
+  return launch(segment_copy_kernel<uint8_t>);
 }
 
 }  // namespace cp
