@@ -3,14 +3,16 @@
 //     dot products and the online max/sum reduced with warp shuffles);
 //   * the fp32 LSE merge of a block partial into the accumulator
 //     (bandwidth-bound, 128-bit loads and stores);
-//   * the segment copy behind the Ulysses seq<->head regroups (bandwidth-bound,
-//     one warp per contiguous segment, 128-bit vectors).
+//   * the segment copy behind the Ulysses seq<->head regroups (bandwidth-bound):
+//     bulk TMA copies through a shared-memory ring when segments are 16-byte
+//     multiples of a few hundred bytes or more, else warps of 128-bit vectors.
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
 
 #include "cp_internal.h"
+#include "cp_ptx.cuh"
 
 namespace cp {
 namespace {
@@ -241,6 +243,122 @@ __global__ void __launch_bounds__(256) segment_copy_kernel(const SegCopy c, int6
   }
 }
 
+// ----------------------------------------------------------------------------
+// Segment copy with bulk TMA copies. One thread per CTA walks a contiguous
+// range of output segments in chunks of K consecutive segments (K * segment
+// bytes <= one ring slot): K bulk loads gather a chunk's segments from their
+// strided sources into a shared-memory slot (completing on the slot's
+// mbarrier), and one bulk store writes the slot to the chunk's contiguous
+// output range. Loads run kBulkSlots - 1 chunks ahead of stores; a slot is
+// refilled only after the store that last read it has finished reading.
+// Every wait is bounded; on expiry the thread records the timeout, waits
+// (bounded) for its in-flight loads and all its stores, and returns.
+// ----------------------------------------------------------------------------
+constexpr int kBulkSlots = 4;
+constexpr uint64_t kCopyWaitTimeoutNs = 1000000000ull;  // 1 s per device-side wait
+constexpr int kBulkSlotBytes = 24 * 1024;
+constexpr int kBulkSmem = kBulkSlots * kBulkSlotBytes;
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Bounded wait for phase `parity` of an mbarrier; false on expiry.
+__device__ __forceinline__ bool bulk_bar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1; !mbar_try_wait(bar, parity); ++n)
+    if ((n & 255u) == 0 && global_timer_ns() - t0 > timeout_ns) return false;
+  return true;
+}
+
+__global__ void __launch_bounds__(32) segment_copy_bulk_kernel(const SegCopy c, int64_t per_cta, int K,
+                                                               uint32_t* err, uint64_t timeout_ns) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t bars[kBulkSlots];
+  if (threadIdx.x != 0) return;
+  const int64_t nseg = c.n0 * c.n1 * c.n2 * c.n3;
+  const int64_t seg_bytes = c.seg_elems * c.elem_bytes;
+  int64_t sg0 = static_cast<int64_t>(blockIdx.x) * per_cta;
+  const int64_t end = sg0 + per_cta < nseg ? sg0 + per_cta : nseg;
+  if (sg0 >= end) return;
+  for (int i = 0; i < kBulkSlots; ++i) mbar_init(smem_addr(&bars[i]), 1);
+  fence_mbar_init();
+  const char* in = static_cast<const char*>(c.in);
+  char* out = static_cast<char*>(c.out);
+  int64_t rest = sg0;
+  int64_t i3 = rest % c.n3;
+  rest /= c.n3;
+  int64_t i2 = rest % c.n2;
+  rest /= c.n2;
+  int64_t i1 = rest % c.n1;
+  int64_t src_el = (rest / c.n1) * c.st0 + i1 * c.st1 + i2 * c.st2 + i3 * c.st3;
+  auto advance = [&]() {  // to the next segment in (i0, i1, i2, i3) order
+    src_el += c.st3;
+    if (++i3 == c.n3) {
+      i3 = 0;
+      src_el += c.st2 - c.n3 * c.st3;
+      if (++i2 == c.n2) {
+        i2 = 0;
+        src_el += c.st1 - c.n2 * c.st2;
+        if (++i1 == c.n1) {
+          i1 = 0;
+          src_el += c.st0 - c.n1 * c.st1;
+        }
+      }
+    }
+  };
+  const int64_t nchunks = (end - sg0 + K - 1) / K;
+  const uint32_t ring0 = smem_addr(ring);
+  int64_t loaded = 0;  // chunks whose loads were issued
+  bool ok = true;
+  for (int64_t ci = 0; ci < nchunks + (kBulkSlots - 1) && ok; ++ci) {
+    if (ci < nchunks) {
+      const int slot = static_cast<int>(ci % kBulkSlots);
+      if (ci >= kBulkSlots) bulk_wait_read_all();  // the store that last read this slot
+      const int64_t first = sg0 + ci * K;
+      const int n = static_cast<int>(end - first < K ? end - first : K);
+      const uint32_t bar = smem_addr(&bars[slot]);
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * seg_bytes));
+      for (int k = 0; k < n; ++k) {
+        bulk_load(ring0 + slot * kBulkSlotBytes + static_cast<uint32_t>(k * seg_bytes), in + src_el * c.elem_bytes,
+                  static_cast<uint32_t>(seg_bytes), bar);
+        advance();
+      }
+      ++loaded;
+    }
+    const int64_t cj = ci - (kBulkSlots - 1);
+    if (cj >= 0 && cj < nchunks) {
+      const int slot = static_cast<int>(cj % kBulkSlots);
+      if (!bulk_bar_wait(smem_addr(&bars[slot]), static_cast<uint32_t>((cj / kBulkSlots) & 1), timeout_ns)) {
+        atomicOr(err, kDevErrTimeout);
+        ok = false;
+        break;
+      }
+      const int64_t first = sg0 + cj * K;
+      const int64_t n = end - first < K ? end - first : K;
+      bulk_store(out + first * seg_bytes, ring0 + slot * kBulkSlotBytes, static_cast<uint32_t>(n * seg_bytes));
+    }
+  }
+  if (!ok) {
+    // let every issued load land before the CTA's shared memory goes away
+    for (int64_t cj = loaded - kBulkSlots < 0 ? 0 : loaded - kBulkSlots; cj < loaded; ++cj)
+      (void)bulk_bar_wait(smem_addr(&bars[cj % kBulkSlots]), static_cast<uint32_t>((cj / kBulkSlots) & 1),
+                          timeout_ns);
+  }
+  bulk_wait_all();
+}
+
 template <int D>
 cudaError_t launch_f32_d(const AttnArgs& a, cudaStream_t s) {
   dim3 grid(a.g.cta_prefix[a.g.n_q], a.H, a.B);
@@ -285,6 +403,23 @@ cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s) {
   uint64_t align = static_cast<uint64_t>(seg_bytes) | reinterpret_cast<uintptr_t>(c.in) |
                    reinterpret_cast<uintptr_t>(c.out);
   for (int64_t st : {c.st0, c.st1, c.st2, c.st3}) align |= static_cast<uint64_t>(st * c.elem_bytes);
+  if (align % 16 == 0 && seg_bytes >= 256 && seg_bytes <= kBulkSlotBytes) {
+    uint32_t* err = device_error_word();
+    if (err == nullptr) return cudaErrorUnknown;
+    static_assert(kBulkSmem <= 227 * 1024, "shared memory budget");
+    cudaError_t e = cudaFuncSetAttribute(segment_copy_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kBulkSmem);
+    if (e != cudaSuccess) return e;
+    const int K = static_cast<int>(kBulkSlotBytes / seg_bytes);
+    // two CTAs per SM (two rings fit in shared memory), at least one chunk each
+    const int64_t chunks = (nseg + K - 1) / K;
+    const int64_t ctas = chunks < 2LL * sms ? chunks : 2LL * sms;
+    const int64_t per_cta = (chunks + ctas - 1) / ctas * K;
+    const int64_t grid = (nseg + per_cta - 1) / per_cta;
+    segment_copy_bulk_kernel<<<static_cast<unsigned>(grid), 32, kBulkSmem, s>>>(c, per_cta, K, err,
+                                                                                 kCopyWaitTimeoutNs);
+    return cudaGetLastError();
+  }
   auto launch = [&](auto kernel) {
     int per_sm = 1;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);

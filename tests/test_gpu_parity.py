@@ -80,6 +80,8 @@ def dev(*ts):
     (3, 1, 9, 6, 4, torch.float32),
     (1, 2, 7, 3, 64, torch.bfloat16),
     (6, 1, 12, 6, 3, torch.bfloat16),        # 6-byte segments: narrow-vector path
+    (2, 1, 6, 128, 128, torch.float32),      # 32 KB segments: larger than a bulk-copy slot
+    (4, 3, 520, 8, 64, torch.bfloat16),      # 256-byte segments, ragged last chunk
 ])
 def test_permutes_bit_exact(U, B, S, H, D, dtype):
     g = torch.Generator().manual_seed(U * 1000 + S)
