@@ -245,6 +245,89 @@ def ulysses_attention(q, k, v, scale: float, ulysses_degree: int):
 
 
 # ---------------------------------------------------------------------------
+# Ulysses Anything ([CP] Ulysses Anything Attention: drops the requirement
+# that the sequence length and the head count be divisible by
+# ulysses_degree; it cannot be combined with Unified Attention, so
+# ring_degree must be 1; [API] ulysses_anything). The pages do not say how
+# the tokens and heads are split. Reading R15: both are split like R5 -
+# balanced, the first S mod U ranks hold one token more and the first H mod U
+# groups one head more. With uneven shards the regroup buffers are ragged, so
+# they are lists of per-rank / per-group arrays:
+#   anything_seq2head: out_g[b, soff_u + s, h, d] = in_u[b, s, hoff_g + h, d]
+#   anything_head2seq: out_u[b, s, hoff_g + h, d] = in_g[b, soff_u + s, h, d]
+# ---------------------------------------------------------------------------
+def balanced_split(n: int, parts: int):
+    """[(offset, length)] of the balanced split of n items into `parts` (R5, R15)."""
+    return ring_shard_table(n, parts, True)
+
+
+def anything_seq2head(x_ranks):
+    """U arrays [B, S_u, H, D] (sequence shards) -> U arrays [B, S, H_g, D] (head groups)."""
+    U = len(x_ranks)
+    B, _, H, D = x_ranks[0].shape
+    S = sum(x.shape[1] for x in x_ranks)
+    seq, heads = balanced_split(S, U), balanced_split(H, U)
+    if [x.shape[1] for x in x_ranks] != [ln for _, ln in seq]:
+        raise ValueError("rank shards are not the balanced split of the sequence")
+    out = []
+    for g, (ho, hl) in enumerate(heads):
+        y = np.empty((B, S, hl, D), dtype=x_ranks[0].dtype)
+        for u, (so, sl) in enumerate(seq):
+            for h in range(hl):
+                y[:, so:so + sl, h, :] = x_ranks[u][:, :, ho + h, :]
+        out.append(y)
+    return out
+
+
+def anything_head2seq(x_groups):
+    """U arrays [B, S, H_g, D] (head groups) -> U arrays [B, S_u, H, D] (sequence shards)."""
+    U = len(x_groups)
+    B, S, _, D = x_groups[0].shape
+    H = sum(x.shape[2] for x in x_groups)
+    seq, heads = balanced_split(S, U), balanced_split(H, U)
+    if [x.shape[2] for x in x_groups] != [ln for _, ln in heads]:
+        raise ValueError("head groups are not the balanced split of the heads")
+    out = []
+    for u, (so, sl) in enumerate(seq):
+        y = np.empty((B, sl, H, D), dtype=x_groups[0].dtype)
+        for g, (ho, hl) in enumerate(heads):
+            for h in range(hl):
+                y[:, :, ho + h, :] = x_groups[g][:, so:so + sl, h, :]
+        out.append(y)
+    return out
+
+
+def anything_head2seq_lse(lse_groups):
+    """U arrays [B, H_g, S] -> [B, H, S]: lse[b, hoff_g + h, s] = lse_g[b, h, s]."""
+    B, _, S = lse_groups[0].shape
+    H = sum(x.shape[1] for x in lse_groups)
+    out = np.empty((B, H, S), dtype=lse_groups[0].dtype)
+    for (ho, hl), x in zip(balanced_split(H, len(lse_groups)), lse_groups):
+        for h in range(hl):
+            out[:, ho + h, :] = x[:, h, :]
+    return out
+
+
+def ulysses_anything_attention(q, k, v, scale: float, ulysses_degree: int):
+    """Ulysses with balanced, possibly uneven token shards and head groups."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, S, H, D = q.shape
+    U = ulysses_degree
+    if U > H:
+        raise ValueError(f"ulysses_degree {U} exceeds the number of heads {H}")
+    seq = balanced_split(S, U)
+    qh, kh, vh = (anything_seq2head([t[:, so:so + sl] for so, sl in seq]) for t in (q, k, v))
+    outs, lses = [], []
+    for g in range(U):
+        o, l = attention(qh[g], kh[g], vh[g], scale)
+        outs.append(o)
+        lses.append(l)
+    out = np.concatenate(anything_head2seq(outs), axis=1)
+    lse = anything_head2seq_lse(lses)
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
 # Unified sequence parallelism ([CP] Unified Attention: an all-to-all
 # redistributes heads and tokens, ring attention runs on the result, then the
 # all-to-all is reversed; the devices form a 2D ulysses x ring grid with
@@ -286,18 +369,22 @@ def cp_attention(q, k, v, scale: float, ring_degree: int = 1, ulysses_degree: in
                  uneven_ok: bool = False):
     """Dispatch on the ContextParallelConfig degrees ([CP] variants table).
 
-    Ring (ring_degree > 1), Ulysses (ulysses_degree > 1), Unified (both > 1),
-    Ring Anything (ring_degree > 1 with uneven_ok; ulysses_degree must be 1).
+    Ring (ring_degree > 1), Ulysses (ulysses_degree > 1), Unified (both > 1).
+    uneven_ok selects an Anything variant: Ring Anything (ring_degree > 1,
+    ulysses_degree == 1) or Ulysses Anything (ulysses_degree > 1,
+    ring_degree == 1); neither combines with the other degree.
     """
     q = _f64(q)
     B, S, H, D = q.shape
     R, U = ring_degree, ulysses_degree
     if R < 1 or U < 1:
         raise ValueError("degrees must be >= 1")
-    if uneven_ok and (U != 1 or R < 2):
-        raise UnsupportedComboError("Ring Anything needs ring_degree > 1 and ulysses_degree == 1")
+    if uneven_ok and (R > 1) == (U > 1):
+        raise UnsupportedComboError("an Anything variant needs exactly one of ring_degree, ulysses_degree > 1")
     if U > H:
         raise ValueError(f"ulysses_degree {U} exceeds the number of heads {H}")
+    if uneven_ok and U > 1:
+        return ulysses_anything_attention(q, k, v, scale, U)
     if U == 1:
         return ring_attention(q, k, v, scale, R, uneven_ok)
     if R == 1:

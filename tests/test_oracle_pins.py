@@ -255,14 +255,14 @@ def test_golden_variant_requirements():
         try:
             if R < 1 or U < 1:
                 raise ValueError
-            if ev and (U != 1 or R < 2):
+            if ev and (R > 1) == (U > 1):
                 raise oracle.UnsupportedComboError
             if U > H:
                 got = "invalid_arg"
                 raise StopIteration
             if U == 1:
                 oracle.ring_shard_table(S, R, ev)
-            elif S % (R * U) or H % U:
+            elif not ev and (S % (R * U) or H % U):
                 raise oracle.NotDivisibleError
             got = "ok"
         except StopIteration:
@@ -416,3 +416,81 @@ def test_planted_permute_mistakes_are_caught(kind):
                 gg = (g + 1) % U if kind == "group_swap" else g
                 y[gg, :, dst, h, :] = x[u, :, :, src_h, :]
     assert not np.array_equal(y, reshape_seq2head(x))
+
+
+# ---------------------------------------------------------------------------
+# Ulysses Anything: ragged regroups (reading R15: balanced token shards and
+# head groups). The balanced split's closed form, offset(u) = u*floor(n/U) +
+# min(u, n mod U), is computed here independently of the oracle's table.
+# ---------------------------------------------------------------------------
+def _bal_off(n, U, u):
+    return u * (n // U) + min(u, n % U)
+
+
+RAGGED = [(1, 37, 7, 3, 4), (2, 10, 5, 4, 3), (1, 9, 6, 4, 2), (3, 4, 3, 3, 1), (1, 13, 24, 5, 2)]
+
+
+@pytest.mark.parametrize("B,S,H,U,D", RAGGED)
+def test_anything_seq2head_elementwise(B, S, H, U, D):
+    x = np.arange(B * S * H * D, dtype=np.int64).reshape(B, S, H, D)  # value = flat index
+    ranks = [x[:, _bal_off(S, U, u):_bal_off(S, U, u + 1)] for u in range(U)]
+    groups = co.anything_seq2head(ranks)
+    for g in range(U):
+        h0, h1 = _bal_off(H, U, g), _bal_off(H, U, g + 1)
+        assert groups[g].shape == (B, S, h1 - h0, D)
+        for b in range(B):
+            for t in range(S):
+                for h in range(h1 - h0):
+                    for d in range(D):
+                        assert groups[g][b, t, h, d] == ((b * S + t) * H + h0 + h) * D + d
+    back = co.anything_head2seq(groups)
+    for u in range(U):
+        assert np.array_equal(back[u], ranks[u])
+
+
+@pytest.mark.parametrize("U", [1, 2, 4])
+def test_anything_regroups_reduce_to_plain_ulysses(U):
+    x = rnd((U, 2, 3, 8, 2), 5)
+    got = co.anything_seq2head(list(x))
+    want = oracle.seq2head(x)
+    assert all(np.array_equal(got[g], want[g]) for g in range(U))
+    assert all(np.array_equal(a, b) for a, b in zip(co.anything_head2seq(got), oracle.head2seq(want)))
+
+
+def test_anything_lse_regroup_elementwise():
+    B, H, S, U = 2, 7, 5, 3
+    lse = [np.arange(B * (_bal_off(H, U, g + 1) - _bal_off(H, U, g)) * S, dtype=np.float64).reshape(B, -1, S) + 1000 * g
+           for g in range(U)]
+    full = co.anything_head2seq_lse(lse)
+    for g in range(U):
+        h0, h1 = _bal_off(H, U, g), _bal_off(H, U, g + 1)
+        assert np.array_equal(full[:, h0:h1, :], lse[g])
+
+
+@pytest.mark.parametrize("B,S,H,U,D", RAGGED + [(1, 24, 8, 4, 3)])
+def test_ulysses_anything_equals_full_attention(B, S, H, U, D):
+    q, k, v = (rnd((B, S, H, D), i + S) for i in range(3))
+    o, l = oracle.cp_attention(q, k, v, 0.4, 1, U, True)
+    ro, rl = oracle.attention(q, k, v, 0.4)
+    assert np.max(np.abs(o - ro)) <= 1e-12 and np.max(np.abs(l - rl)) <= 1e-12
+
+
+@pytest.mark.parametrize("kind", ["floor_split", "head_groups_reversed", "ceil_split"])
+def test_planted_anything_mistakes_are_caught(kind):
+    B, S, H, U, D = 1, 10, 5, 4, 2
+    x = np.arange(B * S * H * D).reshape(B, S, H, D)
+    if kind == "floor_split":      # uneven shards cut at u*S//U instead of the balanced split
+        cut = [u * S // U for u in range(U + 1)]
+    elif kind == "ceil_split":     # ceil-chunking: the last shard takes the shortfall
+        c = -(-S // U)
+        cut = [min(S, u * c) for u in range(U + 1)]
+    else:
+        cut = [_bal_off(S, U, u) for u in range(U + 1)]
+    hcut = [_bal_off(H, U, g) for g in range(U + 1)]
+    if kind == "head_groups_reversed":
+        hcut = [H - c for c in reversed(hcut)]
+    wrong = [np.concatenate([x[:, cut[u]:cut[u + 1], hcut[g]:hcut[g + 1]] for u in range(U)], axis=1)
+             for g in range(U)]
+    right = co.anything_seq2head([x[:, _bal_off(S, U, u):_bal_off(S, U, u + 1)] for u in range(U)])
+    assert any(w.shape != r.shape or not np.array_equal(w, r) for w, r in zip(wrong, right)) or \
+        [cut[u + 1] - cut[u] for u in range(U)] != [_bal_off(S, U, u + 1) - _bal_off(S, U, u) for u in range(U)]
