@@ -217,7 +217,8 @@ def secondary(cpa, dev, flush, stream, peaks):
     del xs, ys, fns
 
     # cp_attention_fwd on the other workloads (fused lap), inputs resident
-    for name in ("flux_ulysses4", "ring_anything3", "video_unified"):
+    for name in ("flux_ulysses4", "ring_anything3", "video_unified", "flux1008_ulysses_anything4",
+                 "ulysses_anything5_heads"):
         w = WORKLOADS[name]
         q, k, v = (t.to(dev) for t in make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed, w.q_mult))
         out = torch.empty((w.B, w.S, w.H, w.D), device=dev)

@@ -16,6 +16,8 @@ from .api import (  # noqa: F401
     cp_lse_merge,
     cp_ring_shard_table,
     cp_status_string,
+    cp_ulysses_anything_head2seq,
+    cp_ulysses_anything_seq2head,
     cp_ulysses_head2seq,
     cp_ulysses_seq2head,
     cp_version,

@@ -37,6 +37,8 @@ SIGNATURES = {
     "cp_lse_merge": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "cp_ulysses_seq2head": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     "cp_ulysses_head2seq": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
+    "cp_ulysses_anything_seq2head": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
+    "cp_ulysses_anything_head2seq": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     "cp_attention_validate": (_i, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "cp_ring_shard_table": (_i, [_i, _i, _i, _ip, _ip]),
     "cp_attention_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),

@@ -104,6 +104,29 @@ def cp_ulysses_head2seq(x_in, x_out, stream=None):
     check(st, "cp_ulysses_head2seq")
 
 
+def _anything(name, x_in, x_out, U, B, S, H, D, stream):
+    _cuda(x_in, x_out)
+    n = B * S * H * D
+    if x_in.numel() != n or x_out.numel() != n or x_out.dtype != x_in.dtype:
+        raise ValueError("both buffers must hold B*S*H*D elements of one dtype")
+    if not (x_in.is_contiguous() and x_out.is_contiguous()):
+        raise ValueError("buffers must be dense")
+    st = getattr(lib(), name)(x_in.data_ptr(), x_out.data_ptr(), U, B, S, H, D, x_in.element_size(),
+                              _stream(stream))
+    check(st, name)
+
+
+def cp_ulysses_anything_seq2head(x_in, x_out, U, B, S, H, D, stream=None):
+    """Ragged regroup: rank blocks [B, S_u, H, D] back to back -> head-group blocks [B, S, H_g, D]
+    back to back (balanced splits of S and H into U; any dtype; flat dense buffers)."""
+    _anything("cp_ulysses_anything_seq2head", x_in, x_out, U, B, S, H, D, stream)
+
+
+def cp_ulysses_anything_head2seq(x_in, x_out, U, B, S, H, D, stream=None):
+    """Inverse of cp_ulysses_anything_seq2head."""
+    _anything("cp_ulysses_anything_head2seq", x_in, x_out, U, B, S, H, D, stream)
+
+
 def cp_attention_validate(B, H, S, D, ring_degree=1, ulysses_degree=1, uneven_ok=False, dtype=torch.bfloat16) -> int:
     """Status code cp_attention_fwd would return on validation (0 = ok). Host only."""
     return lib().cp_attention_validate(B, H, S, D, ring_degree, ulysses_degree, int(bool(uneven_ok)), _DT[dtype])
@@ -196,6 +219,7 @@ def cp_version() -> int:
 
 __all__ = [
     "CpError", "cp_block_attn_fwd", "cp_lse_merge", "cp_ulysses_seq2head", "cp_ulysses_head2seq",
+    "cp_ulysses_anything_seq2head", "cp_ulysses_anything_head2seq",
     "cp_attention_validate", "cp_ring_shard_table", "cp_attention_workspace_size", "cp_attention_launch_count",
     "cp_attention_fwd", "cp_attention_fwd_no_alloc", "cp_check_device_status", "cp_debug_bounded_wait_probe", "cp_status_string", "cp_version",
 ]

@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     blk_b = b_;
   }
   const int h = blk_h, b = blk_b;
+  if (attn_head_is_padding(a, h, b)) return;  // uniform per CTA, before any barrier or TMEM
   const int NT = total_tiles(a.g, r);
 
   if (threadIdx.x == 0) {

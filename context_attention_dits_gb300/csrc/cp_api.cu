@@ -6,10 +6,12 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "cp_attn.h"
 #include "cp_internal.h"
@@ -140,6 +142,8 @@ struct AttnTensors {
   float* out;
   int64_t o_bstride;
   float* lse;  // dense [Bn, H, Sq]
+  int hv_bpg = 1;                  // ragged head groups: batch entries per group
+  int hv_short_from = INT_MAX;     // first group whose last head is padding
 };
 
 cp_status launch_attention(const AttnTensors& t, const RingGeom& g, float scale, cp_dtype dt, DeviceInfo* dev,
@@ -160,6 +164,8 @@ cp_status launch_attention(const AttnTensors& t, const RingGeom& g, float scale,
   a.l_hstride = t.Sq;
   a.err = dev->err;
   a.timeout_ns = kWaitTimeoutNs;
+  a.hv_bpg = t.hv_bpg;
+  a.hv_short_from = t.hv_short_from;
   cudaError_t e;
   if (dt == CP_BF16) {
     CUtensorMap tq, tk, tv;
@@ -203,8 +209,10 @@ struct WsLayout {
 
 WsLayout ws_layout(int B, int H, int S, int D, int R, int U, cp_dtype dt, cp_lap_mode mode) {
   WsLayout w;
-  const size_t n = static_cast<size_t>(B) * S * H * D;
-  const size_t nl = static_cast<size_t>(B) * H * S;
+  // U head groups of ceil(H/U) heads (the last heads of short groups are padding)
+  const size_t Hp = U > 1 ? static_cast<size_t>((H + U - 1) / U) * U : static_cast<size_t>(H);
+  const size_t n = static_cast<size_t>(B) * S * Hp * D;
+  const size_t nl = static_cast<size_t>(B) * Hp * S;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -321,15 +329,68 @@ cp_status cp_ulysses_head2seq(const void* in, void* out, int U, int B, int S, in
   return cp::launch_segment_copy(c, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
+// Ulysses Anything regroups over ragged rank blocks and head groups (balanced
+// splits of S and H into U). Rank u's block [B, S_u, H, D] starts at element
+// B*soff_u*H*D; group g's block [B, S, H_g, D] at element B*S*hoff_g*D.
+static cp_status check_anything(const void* in, const void* out, int U, int B, int S, int H, int D, int eb) {
+  if (U < 1 || B < 0 || S < 0 || H < 1 || D < 1 || U > H || (eb != 1 && eb != 2 && eb != 4 && eb != 8))
+    return CP_ERR_INVALID_ARG;
+  if (B > 0 && S > 0 && (!in || !out)) return CP_ERR_INVALID_ARG;
+  return CP_OK;
+}
+
+static cp_status anything_regroup(const void* in, void* out, int U, int B, int S, int H, int D, int eb,
+                                  bool to_heads, void* stream) {
+  cp_status st = check_anything(in, out, U, B, S, H, D, eb);
+  if (st != CP_OK) return st;
+  if (B == 0 || S == 0) return CP_OK;
+  std::vector<int> so(U), sl(U), ho(U), hl(U);
+  if (shard_table(S, U, true, so.data(), sl.data()) != CP_OK || shard_table(H, U, true, ho.data(), hl.data()) != CP_OK)
+    return CP_ERR_INVALID_ARG;
+  const char* src = static_cast<const char*>(in);
+  char* dst = static_cast<char*>(out);
+  const int64_t HD = static_cast<int64_t>(H) * D;
+  for (int g = 0; g < U; ++g) {
+    const int64_t gD = static_cast<int64_t>(hl[g]) * D;       // elements of a group row
+    const int64_t gbase = static_cast<int64_t>(B) * S * ho[g] * D;
+    for (int u = 0; u < U; ++u) {
+      if (sl[u] == 0) continue;
+      const int64_t rbase = static_cast<int64_t>(B) * so[u] * HD;
+      // rank side: rows (b, s) of pitch H*D, batch stride S_u*H*D, head offset hoff_g
+      const int64_t r_el = rbase + static_cast<int64_t>(ho[g]) * D, r_b = sl[u] * HD;
+      // group side: rows (b, soff_u + s) of pitch H_g*D, batch stride S*H_g*D
+      const int64_t g_el = gbase + static_cast<int64_t>(so[u]) * gD, g_b = S * gD;
+      SegCopy c = to_heads ? SegCopy{src + r_el * eb, dst + g_el * eb, 1, 1, B, sl[u], 0, 0, r_b, HD, gD, eb,
+                                     0, 0, g_b, gD}
+                           : SegCopy{src + g_el * eb, dst + r_el * eb, 1, 1, B, sl[u], 0, 0, g_b, gD, gD, eb,
+                                     0, 0, r_b, HD};
+      if (cp::launch_segment_copy(c, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CP_ERR_CUDA;
+    }
+  }
+  return CP_OK;
+}
+
+cp_status cp_ulysses_anything_seq2head(const void* in, void* out, int U, int B, int S, int H, int D, int elem_bytes,
+                                       void* stream) {
+  return anything_regroup(in, out, U, B, S, H, D, elem_bytes, true, stream);
+}
+
+cp_status cp_ulysses_anything_head2seq(const void* in, void* out, int U, int B, int S, int H, int D, int elem_bytes,
+                                       void* stream) {
+  return anything_regroup(in, out, U, B, S, H, D, elem_bytes, false, stream);
+}
+
 cp_status cp_attention_validate(int B, int H, int S, int D, int ring_degree, int ulysses_degree, int uneven_ok,
                                 cp_dtype dt) {
   cp_status st = check_common(B, H, S, D, dt);
   if (st != CP_OK) return st;
   const int R = ring_degree, U = ulysses_degree;
   if (R < 1 || U < 1 || R > cp::kMaxRanks) return CP_ERR_INVALID_ARG;
-  if (uneven_ok && (U != 1 || R < 2)) return CP_ERR_UNSUPPORTED_COMBO;
+  // an Anything variant: Ring Anything (R > 1, U == 1) or Ulysses Anything (U > 1, R == 1)
+  if (uneven_ok && (R > 1) == (U > 1)) return CP_ERR_UNSUPPORTED_COMBO;
   if (U > H) return CP_ERR_INVALID_ARG;
   if (U == 1) return (S % R && !uneven_ok) ? CP_ERR_NOT_DIVISIBLE : CP_OK;
+  if (uneven_ok) return CP_OK;  // Ulysses Anything: any S and H
   if (H % U || S % (static_cast<int64_t>(R) * U)) return CP_ERR_NOT_DIVISIBLE;
   return CP_OK;
 }
@@ -353,7 +414,8 @@ int cp_attention_launch_count(int B, int H, int S, int D, int ring_degree, int u
   if (B == 0 || S == 0) return 0;
   const int R = ring_degree, U = ulysses_degree;
   int n = (mode == CP_LAP_STEPWISE && R > 1) ? R + (R - 1) : 1;
-  if (U > 1) n += 3 /* seq2head q, k, v */ + 2 /* head2seq out, lse */;
+  if (U > 1 && H % U == 0) n += 3 /* seq2head q, k, v */ + 2 /* head2seq out, lse */;
+  if (U > 1 && H % U != 0) n += 5 * U; /* per head group: q, k, v in; out, lse back */
   return n;
 }
 
@@ -375,10 +437,17 @@ cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* o
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   const int eb = elem_size(dt);
-  const int Hg = H / U, Bn = B * U;
+  // head groups: balanced split of H into U (Ulysses Anything may leave it
+  // uneven); each group is stored with Hg = ceil(H/U) heads, the last head of
+  // a short group being padding that the attention kernels skip
+  const int Hg = (H + U - 1) / U, Bn = B * U;
+  const bool ragged = H % U != 0;
+  std::vector<int> hoff(U), hlen(U);
+  if (shard_table(H, U, true, hoff.data(), hlen.data()) != CP_OK) return CP_ERR_INVALID_ARG;
   const int64_t row = static_cast<int64_t>(Hg) * D;
+  const int64_t grp = static_cast<int64_t>(B) * S * row;  // elements per head group
 
-  // --- Ulysses all-to-all #1 (simulated): global [B,S,H,D] -> [U][B,S,H/U,D] ---
+  // --- Ulysses all-to-all #1 (simulated): global [B,S,H,D] -> [U][B,S,Hg,D] ---
   const void *qa = q, *ka = k, *va = v;
   float* oa = out;
   float* la = lse;
@@ -386,10 +455,21 @@ cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* o
     void* dst[3] = {ws + w.qh, ws + w.kh, ws + w.vh};
     const void* src[3] = {q, k, v};
     for (int i = 0; i < 3; ++i) {
-      // out segments (g, b, t) of Hg*D elements <- in[b, t, g*Hg : (g+1)*Hg, :]
-      SegCopy c{src[i], dst[i], 1, U, B, S, 0, row, static_cast<int64_t>(S) * H * D,
-                static_cast<int64_t>(H) * D, row, eb};
-      if (cp::launch_segment_copy(c, s) != cudaSuccess) return CP_ERR_CUDA;
+      if (!ragged) {
+        // out segments (g, b, t) of Hg*D elements <- in[b, t, g*Hg : (g+1)*Hg, :]
+        SegCopy c{src[i], dst[i], 1, U, B, S, 0, row, static_cast<int64_t>(S) * H * D,
+                  static_cast<int64_t>(H) * D, row, eb};
+        if (cp::launch_segment_copy(c, s) != cudaSuccess) return CP_ERR_CUDA;
+      } else {
+        for (int g = 0; g < U; ++g) {
+          // group g, rows (b, t) of hlen[g]*D elements <- in[b, t, hoff[g] : hoff[g] + hlen[g], :]
+          SegCopy c{static_cast<const char*>(src[i]) + static_cast<int64_t>(hoff[g]) * D * eb,
+                    static_cast<char*>(dst[i]) + g * grp * eb, 1, 1, B, S, 0, 0,
+                    static_cast<int64_t>(S) * H * D, static_cast<int64_t>(H) * D,
+                    static_cast<int64_t>(hlen[g]) * D, eb, 0, 0, S * row, row};
+          if (cp::launch_segment_copy(c, s) != cudaSuccess) return CP_ERR_CUDA;
+        }
+      }
     }
     qa = dst[0];
     ka = dst[1];
@@ -406,6 +486,10 @@ cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* o
     RingGeom g;
     fill_geom(&g, dt, R, off, len, R, off, len, -1);
     AttnTensors t{qa, ka, va, Bn, Hg, D, S, S, bstride, bstride, oa, bstride, la};
+    if (U > 1 && ragged) {
+      t.hv_bpg = B;
+      t.hv_short_from = H % U;
+    }
     if ((st = launch_attention(t, g, scale, dt, dev, s)) != CP_OK) return st;
   } else {
     float* op = reinterpret_cast<float*>(ws + w.op);
@@ -420,11 +504,23 @@ cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* o
   }
 
   // --- Ulysses all-to-all #2 (simulated): [U][B,S,H/U,D] -> [B,S,H,D]; lse [U][B,H/U,S] -> [B,H,S] ---
-  if (U > 1) {
+  if (U > 1 && !ragged) {
     SegCopy co{oa, out, 1, B, S, U, 0, bstride, row, static_cast<int64_t>(B) * bstride, row, 4};
     if (cp::launch_segment_copy(co, s) != cudaSuccess) return CP_ERR_CUDA;
     SegCopy cl{la, lse, 1, B, U, Hg, 0, static_cast<int64_t>(Hg) * S, static_cast<int64_t>(B) * Hg * S, S, S, 4};
     if (cp::launch_segment_copy(cl, s) != cudaSuccess) return CP_ERR_CUDA;
+  } else if (U > 1) {
+    for (int g = 0; g < U; ++g) {
+      // out[b, t, hoff[g] + h, :] <- group g row (b, t), real heads only
+      SegCopy co{oa + g * grp, out + static_cast<int64_t>(hoff[g]) * D, 1, 1, B, S, 0, 0, S * row, row,
+                 static_cast<int64_t>(hlen[g]) * D, 4, 0, 0, static_cast<int64_t>(S) * H * D,
+                 static_cast<int64_t>(H) * D};
+      if (cp::launch_segment_copy(co, s) != cudaSuccess) return CP_ERR_CUDA;
+      // lse[b, hoff[g] + h, :] <- group g lse[b, h, :]
+      SegCopy cl{la + static_cast<int64_t>(g) * B * Hg * S, lse + static_cast<int64_t>(hoff[g]) * S, 1, 1, B,
+                 hlen[g], 0, 0, static_cast<int64_t>(Hg) * S, S, S, 4, 0, 0, static_cast<int64_t>(H) * S, S};
+      if (cp::launch_segment_copy(cl, s) != cudaSuccess) return CP_ERR_CUDA;
+    }
   }
   return CP_OK;
 }

@@ -51,7 +51,17 @@ struct AttnArgs {
   // device error word and the bound on each device-side wait
   uint32_t* err;
   uint64_t timeout_ns;
+  // ragged head groups (Ulysses Anything): batch entries come in groups of
+  // hv_bpg, and groups from hv_short_from on have H - 1 real heads (head H - 1
+  // is padding and is skipped). hv_bpg = 1, hv_short_from = INT_MAX: none.
+  int hv_bpg;
+  int hv_short_from;
 };
+
+// Whether (head h, batch entry b) is padding of a ragged head group.
+__host__ __device__ inline bool attn_head_is_padding(const AttnArgs& a, int h, int b) {
+  return h == a.H - 1 && b / a.hv_bpg >= a.hv_short_from;
+}
 
 // Tensor-core work items of a shard of `rows` query rows: tile pairs, plus one
 // single tile when the tile count is odd. All pairs of all shards are launched
@@ -70,9 +80,10 @@ cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_lse_merge(float* out_acc, float* lse_acc, const float* out_blk, const float* lse_blk,
                              int B, int H, int S, int D, cudaStream_t s);
 
-// Copy of n0*n1*n2*n3 segments of seg_elems elements each: output segments are
-// contiguous in (i0, i1, i2, i3) order; the input segment (i0, i1, i2, i3)
-// starts at element i0*st0 + i1*st1 + i2*st2 + i3*st3.
+// Copy of n0*n1*n2*n3 segments of seg_elems elements each: the input segment
+// (i0, i1, i2, i3) starts at element i0*st0 + i1*st1 + i2*st2 + i3*st3. The
+// output segment starts at i0*ost0 + i1*ost1 + i2*ost2 + i3*ost3, or, when
+// every ost is 0, output segments are contiguous in (i0, i1, i2, i3) order.
 struct SegCopy {
   const void* in;
   void* out;
@@ -80,6 +91,7 @@ struct SegCopy {
   int64_t st0, st1, st2, st3;
   int64_t seg_elems;
   int elem_bytes;
+  int64_t ost0, ost1, ost2, ost3;
 };
 // Picks the widest vector (16, 8, 4 or 1 bytes) that every segment start, the
 // segment length and both base pointers allow.

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(32 * kF32RowsPerCta) attn_fwd_f32_kernel(const
   constexpr int NPL = D / 32;  // elements of a row per lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (attn_head_is_padding(a, h, b)) return;
   int r = 0;
   while (r + 1 < a.g.n_q && a.g.cta_prefix[r + 1] <= item) ++r;
   const int row = (item - a.g.cta_prefix[r]) * kF32RowsPerCta + warp;
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(256) segment_copy_kernel(const SegCopy c, int6
   int64_t sg = (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * per_warp;
   const int64_t end = sg + per_warp < nseg ? sg + per_warp : nseg;
   if (sg >= end) return;
+  const bool out_contig = (c.ost0 | c.ost1 | c.ost2 | c.ost3) == 0;
   int64_t rest = sg;
   int64_t i3 = rest % c.n3;
   rest /= c.n3;
@@ -197,17 +199,22 @@ __global__ void __launch_bounds__(256) segment_copy_kernel(const SegCopy c, int6
   rest /= c.n2;
   int64_t i1 = rest % c.n1;
   int64_t src_el = (rest / c.n1) * c.st0 + i1 * c.st1 + i2 * c.st2 + i3 * c.st3;
+  int64_t dst_el = (rest / c.n1) * c.ost0 + i1 * c.ost1 + i2 * c.ost2 + i3 * c.ost3;
   auto advance = [&]() {  // to the next segment in (i0, i1, i2, i3) order
     src_el += c.st3;
+    dst_el += c.ost3;
     if (++i3 == c.n3) {
       i3 = 0;
       src_el += c.st2 - c.n3 * c.st3;
+      dst_el += c.ost2 - c.n3 * c.ost3;
       if (++i2 == c.n2) {
         i2 = 0;
         src_el += c.st1 - c.n2 * c.st2;
+        dst_el += c.ost1 - c.n2 * c.ost2;
         if (++i1 == c.n1) {
           i1 = 0;
           src_el += c.st0 - c.n1 * c.st1;
+          dst_el += c.ost0 - c.n1 * c.ost1;
         }
       }
     }
@@ -220,7 +227,7 @@ __global__ void __launch_bounds__(256) segment_copy_kernel(const SegCopy c, int6
     for (int k = 0; k < kCopySegs; ++k) {
       ok[k] = sg + k < end;
       src[k] = reinterpret_cast<const V*>(in + src_el * c.elem_bytes);
-      dst[k] = reinterpret_cast<V*>(out + (sg + k) * seg_bytes);
+      dst[k] = reinterpret_cast<V*>(out + (out_contig ? (sg + k) * seg_bytes : dst_el * c.elem_bytes));
       if (ok[k]) advance();
     }
     for (int64_t base = 0; base < nv; base += 32 * kCopyVec) {
@@ -402,8 +409,15 @@ cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   uint64_t align = static_cast<uint64_t>(seg_bytes) | reinterpret_cast<uintptr_t>(c.in) |
                    reinterpret_cast<uintptr_t>(c.out);
-  for (int64_t st : {c.st0, c.st1, c.st2, c.st3}) align |= static_cast<uint64_t>(st * c.elem_bytes);
-  if (align % 16 == 0 && seg_bytes >= 256 && seg_bytes <= kBulkSlotBytes) {
+  for (int64_t st : {c.st0, c.st1, c.st2, c.st3, c.ost0, c.ost1, c.ost2, c.ost3})
+    align |= static_cast<uint64_t>(st * c.elem_bytes);
+  // output strides that describe the contiguous layout allow the bulk path
+  // (a stride of a dimension of extent 1 never matters)
+  const int64_t nat3 = c.seg_elems, nat2 = c.n3 * nat3, nat1 = c.n2 * nat2, nat0 = c.n1 * nat1;
+  const bool natural = (c.n3 == 1 || c.ost3 == nat3) && (c.n2 == 1 || c.ost2 == nat2) &&
+                       (c.n1 == 1 || c.ost1 == nat1) && (c.n0 == 1 || c.ost0 == nat0);
+  const bool out_contig = (c.ost0 | c.ost1 | c.ost2 | c.ost3) == 0 || natural;
+  if (out_contig && align % 16 == 0 && seg_bytes >= 256 && seg_bytes <= kBulkSlotBytes) {
     uint32_t* err = device_error_word();
     if (err == nullptr) return cudaErrorUnknown;
     static_assert(kBulkSmem <= 227 * 1024, "shared memory budget");
@@ -416,7 +430,9 @@ cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s) {
     const int64_t ctas = chunks < 2LL * sms ? chunks : 2LL * sms;
     const int64_t per_cta = (chunks + ctas - 1) / ctas * K;
     const int64_t grid = (nseg + per_cta - 1) / per_cta;
-    segment_copy_bulk_kernel<<<static_cast<unsigned>(grid), 32, kBulkSmem, s>>>(c, per_cta, K, err,
+    SegCopy cc = c;
+    cc.ost0 = cc.ost1 = cc.ost2 = cc.ost3 = 0;  // contiguous output
+    segment_copy_bulk_kernel<<<static_cast<unsigned>(grid), 32, kBulkSmem, s>>>(cc, per_cta, K, err,
                                                                                  kCopyWaitTimeoutNs);
     return cudaGetLastError();
   }

@@ -131,13 +131,44 @@ cp_status cp_ulysses_head2seq(const void* in, void* out, int U, int B, int S, in
                               int elem_bytes, void* stream);
 
 /*
+ * Ulysses Anything regroups ("Paralelismo de contexto", section "Ulysses
+ * Anything Attention": the sequence length and the head count need not be
+ * divisible by ulysses_degree). Tokens and heads are both split into U
+ * balanced shards (this library's reading; cp_ring_shard_table with
+ * uneven_ok gives both tables): rank u holds tokens [soff_u, soff_u + S_u),
+ * group g holds heads [hoff_g, hoff_g + H_g), the first S mod U ranks and the
+ * first H mod U groups one longer.
+ *
+ * Layouts (both buffers hold B*S*H*D elements of elem_bytes bytes, dense):
+ *   sequence-sharded: rank blocks back to back, block u = [B, S_u, H, D]
+ *                     starting at element B*soff_u*H*D;
+ *   head-grouped:     group blocks back to back, block g = [B, S, H_g, D]
+ *                     starting at element B*S*hoff_g*D.
+ *   seq2head: grp_g[b, soff_u + s, h, d] = rank_u[b, s, hoff_g + h, d]
+ *   head2seq: rank_u[b, s, hoff_g + h, d] = grp_g[b, soff_u + s, h, d]
+ * Bit copies (any element type of 1, 2, 4 or 8 bytes). Requires
+ * 1 <= U <= H (INVALID_ARG otherwise); in and out must not overlap. With S
+ * and H divisible by U the layouts and the result equal cp_ulysses_seq2head /
+ * cp_ulysses_head2seq. Asynchronous on `stream`; launch errors -> CP_ERR_CUDA.
+ */
+cp_status cp_ulysses_anything_seq2head(const void* in, void* out, int U, int B, int S, int H, int D,
+                                       int elem_bytes, void* stream);
+cp_status cp_ulysses_anything_head2seq(const void* in, void* out, int U, int B, int S, int H, int D,
+                                       int elem_bytes, void* stream);
+
+/*
  * Host-only: the status cp_attention_fwd would return for these sizes and
  * flags before touching any pointer (the requirements table of the
  * "Paralelismo de contexto" page):
  *   ring needs S % ring_degree == 0 unless uneven_ok (Ring Anything);
- *   Ulysses needs S and H divisible by ulysses_degree, ulysses_degree <= H;
- *   unified (both > 1) needs S % (ring_degree*ulysses_degree) == 0;
- *   uneven_ok needs ring_degree > 1 and ulysses_degree == 1.
+ *   Ulysses needs S and H divisible by ulysses_degree unless uneven_ok
+ *   (Ulysses Anything), and ulysses_degree <= H always;
+ *   unified (both > 1) needs S % (ring_degree*ulysses_degree) == 0 and
+ *   H % ulysses_degree == 0;
+ *   uneven_ok selects an Anything variant and needs exactly one of
+ *   ring_degree, ulysses_degree > 1 ("Ulysses Anything Attention": not with
+ *   Unified, ring_degree 1; ContextParallelConfig.ring_anything:
+ *   ulysses_degree 1).
  * Checks, in order: sizes/D/dtype/degrees >= 1 (INVALID_ARG), the uneven_ok
  * combination (UNSUPPORTED_COMBO), ulysses_degree > H (INVALID_ARG), then
  * divisibility (NOT_DIVISIBLE).
@@ -172,7 +203,10 @@ int cp_attention_launch_count(int B, int H, int S, int D, int ring_degree, int u
  *     (Ring Anything);
  *   ulysses_degree > 1, ring_degree == 1: seq2head of q, k, v into the
  *     workspace, attention per head group over all S tokens, head2seq of out
- *     and lse;
+ *     and lse; with uneven_ok (Ulysses Anything) S and H may be indivisible
+ *     by ulysses_degree: the head groups are the balanced split of H, each
+ *     stored with ceil(H/U) heads, and the kernels skip a short group's last
+ *     (padding) head;
  *   both > 1 (unified): the same regroups, with a ring lap of ring_degree
  *     ranks over each head group's sequence (device (r, u) holds token chunk
  *     r*ulysses_degree + u; ring row r holds tokens [r*S/R, (r+1)*S/R)).

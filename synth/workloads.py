@@ -56,6 +56,12 @@ WORKLOADS = {
         Workload("ring_anything3", B=2, H=24, S=4607, D=128, dtype="bf16", ring_degree=3,
                  ulysses_degree=1, uneven_ok=True, seed=3,
                  description="Ring Anything: S not divisible, shards 1536/1536/1535"),
+        Workload("flux1008_ulysses_anything4", B=1, H=24, S=4481, D=128, dtype="bf16", ring_degree=1,
+                 ulysses_degree=4, uneven_ok=True, seed=5,
+                 description="Ulysses Anything at a 1008x1008 image (512 + 63^2 = 4481 tokens): shards 1121/1120/1120/1120"),
+        Workload("ulysses_anything5_heads", B=1, H=24, S=4608, D=128, dtype="bf16", ring_degree=1,
+                 ulysses_degree=5, uneven_ok=True, seed=6,
+                 description="Ulysses Anything with 24 heads over 5 groups (5/5/5/5/4) and 4608 tokens (922/922/922/921/921)"),
         Workload("video_unified", B=1, H=24, S=32768, D=128, dtype="bf16", ring_degree=2,
                  ulysses_degree=4, uneven_ok=False, seed=4,
                  description="video-length unified grid: ring 2 x Ulysses 4 (16384-token ring blocks, 6-head groups)"),

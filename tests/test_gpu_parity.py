@@ -100,6 +100,36 @@ def test_permutes_bit_exact(U, B, S, H, D, dtype):
 
 
 # ----------------------------------------------------------------------------
+# Ulysses Anything regroups: bit-exact against the ragged oracle permute
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("U,B,S,H,D,dtype", [
+    (4, 1, 4481, 24, 128, torch.bfloat16),  # FLUX 1008x1008: tokens 1121/1120/1120/1120
+    (5, 1, 4608, 24, 128, torch.float32),   # heads 5/5/5/5/4 (3 KB and 2.5 KB rows)
+    (3, 2, 10, 7, 64, torch.float32),
+    (4, 1, 9, 5, 128, torch.bfloat16),
+    (2, 3, 7, 3, 8, torch.float32),
+    (3, 1, 2, 4, 16, torch.bfloat16),       # fewer tokens than ranks: an empty shard
+])
+def test_anything_permutes_bit_exact(U, B, S, H, D, dtype):
+    from oracle import cp_oracle as co
+    iv = torch.int16 if dtype == torch.bfloat16 else torch.int32
+    g = torch.Generator().manual_seed(U * 100 + S)
+    x = torch.randn((B, S, H, D), generator=g).to(dtype)
+    seq = co.balanced_split(S, U)
+    ranks = [x[:, o:o + n].contiguous() for o, n in seq]
+    flat_in = torch.cat([r.reshape(-1) for r in ranks])
+    want_groups = co.anything_seq2head([r.view(iv).numpy() for r in ranks])
+    want = np.concatenate([w.reshape(-1) for w in want_groups])
+    dx = flat_in.cuda()
+    y = torch.empty_like(dx)
+    cpa().cp_ulysses_anything_seq2head(dx, y, U, B, S, H, D)
+    assert np.array_equal(y.cpu().view(iv).numpy(), want)
+    back = torch.empty_like(dx)
+    cpa().cp_ulysses_anything_head2seq(y, back, U, B, S, H, D)
+    assert torch.equal(back.cpu().view(iv), flat_in.view(iv))
+
+
+# ----------------------------------------------------------------------------
 # LSE merge
 # ----------------------------------------------------------------------------
 @pytest.mark.parametrize("B,H,S,D,ninf", [(1, 24, 4608, 128, 0), (2, 3, 37, 64, 10), (1, 5, 9, 4, 6), (3, 1, 1, 8, 1)])
@@ -234,7 +264,8 @@ def workload_reference(name):
     return _ORACLE_CACHE[name]
 
 
-@pytest.mark.parametrize("name", ["tiny_ring", "flux_ring4", "flux_ulysses4", "flux_ulysses4_qx8", "ring_anything3"])
+@pytest.mark.parametrize("name", ["tiny_ring", "flux_ring4", "flux_ulysses4", "flux_ulysses4_qx8", "ring_anything3",
+                                  "flux1008_ulysses_anything4", "ulysses_anything5_heads"])
 @pytest.mark.parametrize("mode", ["fused", "stepwise"])
 def test_cp_attention_workloads_full_oracle(name, mode):
     w = WORKLOADS[name]
@@ -260,6 +291,9 @@ def test_cp_attention_video_unified_sampled_rows(mode):
     (1, 4, 129, 128, 1, 1, False),    # plain attention through the driver
     (1, 2, 3, 64, 4, 1, True),        # more ranks than tokens: one empty shard
     (1, 8, 520, 128, 4, 2, False),    # unified 4 x 2 with ragged tiles (65-token chunks)
+    (2, 7, 300, 64, 1, 3, True),      # Ulysses Anything: heads 3/2/2, tokens 100 x 3
+    (1, 5, 129, 128, 1, 4, True),     # Ulysses Anything: heads 2/1/1/1, tokens 33/32/32/32
+    (1, 24, 130, 128, 1, 5, True),    # Ulysses Anything: heads 5/5/5/5/4, tokens 26 x 5
 ])
 @pytest.mark.parametrize("mode", ["fused", "stepwise"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
