@@ -495,24 +495,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv_l = NT > 0 ? 1.f / l : 0.f;
         const float lse_v = NT > 0 ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
         if (row < rows_valid) a.lse[b * a.l_bstride + h * a.l_hstride + tok0 + row] = lse_v;
-        // stage 32 rows x 32 fp32 per warp in this tile's (now idle) Q buffer, 128B-swizzled,
-        // then store 4 rows x 128 contiguous bytes per warp instruction
-        float* stage = reinterpret_cast<float*>(smem + L::kOffQ + i * L::kQTile + wq * 4096);
-        float* out_b = a.out + b * a.o_bstride + static_cast<int64_t>(h) * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          if (NT > 0) {
-            tmem_ld32(t_o + c * 32, o);
-            tmem_wait_ld();
-          } else {
+        // all of O's row from TMEM at once, then per 32-column chunk: stage 32
+        // rows x 32 fp32 per warp in this tile's (now idle) Q buffer, 128B-
+        // swizzled (double-buffered where the buffer has room), and store 4
+        // rows x 128 contiguous bytes per warp instruction
+        uint32_t o[D];
+        if (NT > 0) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = 0u;
-          }
+          for (int c = 0; c < D / 32; ++c) tmem_ld32(t_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < D; ++e) o[e] = 0u;
+        }
+        float* out_b = a.out + b * a.o_bstride + static_cast<int64_t>(h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          // 8 KB per warp (two 4 KB buffers) when the Q tile has 32 KB, else one buffer
+          constexpr int kWarpStage = L::kQTile / 4 >= 8192 ? 8192 : 4096;
+          float* stage = reinterpret_cast<float*>(smem + L::kOffQ + i * L::kQTile + wq * kWarpStage +
+                                                  (kWarpStage == 8192 ? (c & 1) * 4096 : 0));
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
-            float4 val = make_float4(__uint_as_float(o[4 * q4]) * inv_l, __uint_as_float(o[4 * q4 + 1]) * inv_l,
-                                     __uint_as_float(o[4 * q4 + 2]) * inv_l, __uint_as_float(o[4 * q4 + 3]) * inv_l);
+            const uint32_t* oc = &o[c * 32 + 4 * q4];
+            float4 val = make_float4(__uint_as_float(oc[0]) * inv_l, __uint_as_float(oc[1]) * inv_l,
+                                     __uint_as_float(oc[2]) * inv_l, __uint_as_float(oc[3]) * inv_l);
             *reinterpret_cast<float4*>(stage + lane * 32 + ((q4 ^ (lane & 7)) * 4)) = val;
           }
           __syncwarp();
@@ -525,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (grow < rows_valid)
               *reinterpret_cast<float4*>(out_b + static_cast<int64_t>(tok0 + grow) * a.o_sstride + c * 32 + q4 * 4) = val;
           }
-          __syncwarp();
+          __syncwarp();  // the buffer is read before it is staged again
         }
       }
     }
