@@ -67,7 +67,7 @@ struct Smem {
   static constexpr int kOffK = kOffQ + 2 * kQTile;
   static constexpr int kOffV = kOffK + kStages * kKVTile;
   static constexpr int kOffBar = kOffV + kStages * kKVTile;
-  static constexpr int kNumBars = 16;
+  static constexpr int kNumBars = 17;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   // slack to align the base to 1024 bytes; at least 116 KB so that two CTAs
@@ -86,6 +86,7 @@ enum : int {
   kBarPFull = 11,  // +tile
   kBarOFull = 13,  // +tile
   kBarDrain = 15,
+  kBarQFull1 = 16,  // Q tile 1 (Q tile 0 completes kBarQFull)
 };
 
 __device__ __forceinline__ int ring_block(const RingGeom& g, int r, int t) {
@@ -238,13 +239,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tv);
       }
       int k_issued[2] = {0, 0}, v_issued[2] = {0, 0};
-      if (leader) {
-        mbar_arrive_expect_tx(bar(kBarQFull), nq * L::kQTile);
-        for (int i = 0; i < nq; ++i)
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(sb + L::kOffQ + i * L::kQTile + c * L::kHalf, &tq, bar(kBarQFull), c * 64, h,
-                        qrow[i], b);
-      }
+      // Q tile 0 and K(0) first, so that S_0(0) can start while Q tile 1
+      // is still on its way (each Q tile completes its own barrier)
+      auto load_q = [&](int i) {
+        if (!leader) return;
+        const uint32_t qb = bar(i == 0 ? kBarQFull : kBarQFull1);
+        mbar_arrive_expect_tx(qb, L::kQTile);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sb + L::kOffQ + i * L::kQTile + c * L::kHalf, &tq, qb, c * 64, h, qrow[i], b);
+      };
+      load_q(0);
       KvCursor cur;
       cur.init(a.g, r);
       for (int it = 0; it < NT; ++it) {
@@ -258,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         cur.kv0(), b);
         }
         ++k_issued[s];
+        if (it == 0 && nq == 2) load_q(1);
         if (!mbar_wait_bounded(bar(kBarVEmpty + s), ph ^ 1, abort_flag, a.err, tmo)) break;
         if (leader) {
           mbar_arrive_expect_tx(bar(kBarVFull + s), L::kKVTile);
@@ -271,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) {
         // let every issued copy land before the CTA's shared memory goes away
         drain_wait(bar(kBarQFull), 0, tmo);
+        if (nq == 2 && k_issued[0] > 0) drain_wait(bar(kBarQFull1), 0, tmo);
         for (int s = 0; s < 2; ++s) {
           if (k_issued[s]) drain_wait(bar(kBarKFull + s), (k_issued[s] - 1) & 1, tmo);
           if (v_issued[s]) drain_wait(bar(kBarVFull + s), (v_issued[s] - 1) & 1, tmo);
@@ -319,11 +325,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait_bounded(bar(kBarQFull), 0, abort_flag, a.err, tmo) &&
                 mbar_wait_bounded(bar(kBarKFull), 0, abort_flag, a.err, tmo);
       if (ok) {
-        for (int i = 0; i < nq; ++i) {
+        for (int i = 0; i < nq && ok; ++i) {
+          if (i == 1 && !mbar_wait_bounded(bar(kBarQFull1), 0, abort_flag, a.err, tmo)) {
+            ok = false;
+            break;
+          }
           issue_s(i, 0);
           commit(bar(kBarSFull + i));
         }
-        commit(bar(kBarKEmpty));
+        if (ok) commit(bar(kBarKEmpty));
       }
       // The tensor pipe queues about one MMA: whatever this thread does
       // between two MMA groups leaves the pipe idle. Each step therefore
