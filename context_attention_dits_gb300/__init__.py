@@ -6,7 +6,9 @@ include/cp_attn.h); this package is its build script and a thin torch binding.
 from .api import (  # noqa: F401
     CpError,
     cp_attention_fwd,
+    cp_attention_fwd_host,
     cp_attention_fwd_no_alloc,
+    cp_attention_host_buffer_size,
     cp_attention_launch_count,
     cp_attention_validate,
     cp_attention_workspace_size,

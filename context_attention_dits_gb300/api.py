@@ -178,6 +178,38 @@ def cp_attention_fwd(q, k, v, out, lse, scale: float, ring_degree: int = 1, ulys
     check(st, "cp_attention_fwd")
 
 
+def cp_attention_host_buffer_size(B, H, S, D, ring_degree=1, ulysses_degree=1, dtype=torch.bfloat16,
+                                  mode="fused") -> int:
+    return int(lib().cp_attention_host_buffer_size(B, H, S, D, ring_degree, ulysses_degree, _DT[dtype], _mode(mode)))
+
+
+def cp_attention_fwd_host(q, k, v, out, lse, scale: float, ring_degree: int = 1, ulysses_degree: int = 1,
+                          uneven_ok: bool = False, dev_buffer=None, mode="fused", head_chunks: int = 4,
+                          stream=None):
+    """cp_attention_fwd over host (CPU, ideally pinned) tensors q, k, v [B,S,H,D], out [B,S,H,D] f32 and
+    lse [B,H,S] f32, with transfers overlapping compute over head chunks. dev_buffer: a CUDA uint8 tensor
+    of at least cp_attention_host_buffer_size(...) bytes (allocated here through torch when None).
+    Returns without waiting; the results are in out, lse once `stream` reaches this point."""
+    for t in (q, k, v, out, lse):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, out, lse must be dense host tensors")
+    B, S, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape or out.shape != (B, S, H, D) or lse.shape != (B, H, S):
+        raise ValueError("shape mismatch")
+    if k.dtype != q.dtype or v.dtype != q.dtype or out.dtype != torch.float32 or lse.dtype != torch.float32:
+        raise ValueError("dtype mismatch")
+    need = cp_attention_host_buffer_size(B, H, S, D, ring_degree, ulysses_degree, q.dtype, mode)
+    if dev_buffer is None:
+        dev_buffer = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    _cuda(dev_buffer)
+    st = lib().cp_attention_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                     B, H, S, D, float(scale), ring_degree, ulysses_degree, int(bool(uneven_ok)),
+                                     dev_buffer.data_ptr(), dev_buffer.numel(), _dt(q), _mode(mode), head_chunks,
+                                     _stream(stream))
+    check(st, "cp_attention_fwd_host")
+    return dev_buffer
+
+
 def cp_attention_fwd_no_alloc(q, k, v, out, lse, scale: float, ring_degree: int = 1, ulysses_degree: int = 1,
                               uneven_ok: bool = False, mode="fused", stream=None):
     """cp_attention_fwd with the library's built-in 64 MiB device workspace (no allocation).
@@ -221,5 +253,5 @@ __all__ = [
     "CpError", "cp_block_attn_fwd", "cp_lse_merge", "cp_ulysses_seq2head", "cp_ulysses_head2seq",
     "cp_ulysses_anything_seq2head", "cp_ulysses_anything_head2seq",
     "cp_attention_validate", "cp_ring_shard_table", "cp_attention_workspace_size", "cp_attention_launch_count",
-    "cp_attention_fwd", "cp_attention_fwd_no_alloc", "cp_check_device_status", "cp_debug_bounded_wait_probe", "cp_status_string", "cp_version",
+    "cp_attention_fwd", "cp_attention_fwd_no_alloc", "cp_attention_fwd_host", "cp_attention_host_buffer_size", "cp_check_device_status", "cp_debug_bounded_wait_probe", "cp_status_string", "cp_version",
 ]

@@ -78,15 +78,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 [Bn, S, H, D] with batch stride bstride elements; box = 64 columns x
-// 128 tokens of one head, 128-byte swizzle (the K-major operand layout the
-// MMA descriptors expect).
-bool make_tmap_bf16(CUtensorMap* m, const void* base, int D, int H, int S, int Bn, int64_t bstride) {
+// bf16 [Bn, S, H, D] with token stride row and batch stride bstride elements
+// (row = H*D for a dense tensor; larger for a range of its heads); box = 64
+// columns x 128 tokens of one head, 128-byte swizzle (the K-major operand
+// layout the MMA descriptors expect).
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int D, int H, int S, int Bn, int64_t row, int64_t bstride) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
                         static_cast<cuuint64_t>(Bn)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(row) * 2,
                            static_cast<cuuint64_t>(bstride) * 2};
   cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(cp::kTileM), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -141,9 +142,11 @@ struct AttnTensors {
   int64_t q_bstride, kv_bstride;
   float* out;
   int64_t o_bstride;
-  float* lse;  // dense [Bn, H, Sq]
+  float* lse;  // [Bn, H, Sq], head stride Sq
   int hv_bpg = 1;                  // ragged head groups: batch entries per group
   int hv_short_from = INT_MAX;     // first group whose last head is padding
+  int64_t row = 0;                 // token stride of q, k, v and out in elements (0: H*D)
+  int64_t l_bstride = 0;           // batch stride of lse in elements (0: H*Sq)
 };
 
 cp_status launch_attention(const AttnTensors& t, const RingGeom& g, float scale, cp_dtype dt, DeviceInfo* dev,
@@ -158,9 +161,10 @@ cp_status launch_attention(const AttnTensors& t, const RingGeom& g, float scale,
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.out = t.out;
   a.o_bstride = t.o_bstride;
-  a.o_sstride = static_cast<int64_t>(t.H) * t.D;
+  const int64_t row = t.row ? t.row : static_cast<int64_t>(t.H) * t.D;
+  a.o_sstride = row;
   a.lse = t.lse;
-  a.l_bstride = static_cast<int64_t>(t.H) * t.Sq;
+  a.l_bstride = t.l_bstride ? t.l_bstride : static_cast<int64_t>(t.H) * t.Sq;
   a.l_hstride = t.Sq;
   a.err = dev->err;
   a.timeout_ns = kWaitTimeoutNs;
@@ -169,12 +173,12 @@ cp_status launch_attention(const AttnTensors& t, const RingGeom& g, float scale,
   cudaError_t e;
   if (dt == CP_BF16) {
     CUtensorMap tq, tk, tv;
-    if (!make_tmap_bf16(&tq, t.q, t.D, t.H, t.Sq, t.Bn, t.q_bstride)) return CP_ERR_CUDA;
+    if (!make_tmap_bf16(&tq, t.q, t.D, t.H, t.Sq, t.Bn, row, t.q_bstride)) return CP_ERR_CUDA;
     const bool kv_empty = t.Skv == 0;
-    if (!make_tmap_bf16(&tk, kv_empty ? t.q : t.k, t.D, t.H, kv_empty ? t.Sq : t.Skv, t.Bn,
+    if (!make_tmap_bf16(&tk, kv_empty ? t.q : t.k, t.D, t.H, kv_empty ? t.Sq : t.Skv, t.Bn, row,
                         kv_empty ? t.q_bstride : t.kv_bstride))
       return CP_ERR_CUDA;
-    if (!make_tmap_bf16(&tv, kv_empty ? t.q : t.v, t.D, t.H, kv_empty ? t.Sq : t.Skv, t.Bn,
+    if (!make_tmap_bf16(&tv, kv_empty ? t.q : t.v, t.D, t.H, kv_empty ? t.Sq : t.Skv, t.Bn, row,
                         kv_empty ? t.q_bstride : t.kv_bstride))
       return CP_ERR_CUDA;
     e = cp::launch_attn_tc(a, tq, tk, tv, s);
@@ -183,9 +187,9 @@ cp_status launch_attention(const AttnTensors& t, const RingGeom& g, float scale,
     a.kf = static_cast<const float*>(t.k);
     a.vf = static_cast<const float*>(t.v);
     a.q_bstride = t.q_bstride;
-    a.q_sstride = static_cast<int64_t>(t.H) * t.D;
+    a.q_sstride = row;
     a.kv_bstride = t.kv_bstride;
-    a.kv_sstride = static_cast<int64_t>(t.H) * t.D;
+    a.kv_sstride = row;
     e = cp::launch_attn_f32(a, s);
   }
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
@@ -522,6 +526,170 @@ cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* o
       if (cp::launch_segment_copy(cl, s) != cudaSuccess) return CP_ERR_CUDA;
     }
   }
+  return CP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// cp_attention_fwd over host buffers: copies in, attention, copies out, with
+// the head range split into chunks whose copies overlap the other chunks'
+// attention (two copy streams of the library, one per direction).
+// ---------------------------------------------------------------------------
+constexpr int kMaxHostChunks = 16;
+
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, out_done = nullptr;
+  cudaEvent_t in_done[kMaxHostChunks] = {}, comp_done[kMaxHostChunks] = {};
+  std::mutex mu;
+};
+static HostPipe g_pipe[kMaxDevices];
+
+// Device buffer of cp_attention_fwd_host: q, k, v (dt), out, lse (fp32), then
+// the workspace of cp_attention_fwd; every piece 256-byte aligned.
+struct HostLayout {
+  size_t q = 0, k = 0, v = 0, out = 0, lse = 0, ws = 0, ws_bytes = 0, total = 0;
+};
+
+static HostLayout host_layout(int B, int H, int S, int D, int R, int U, cp_dtype dt, cp_lap_mode mode) {
+  HostLayout h;
+  const size_t n = static_cast<size_t>(B) * S * H * D;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = round_up(o + bytes, 256);
+    return at;
+  };
+  h.q = take(n * elem_size(dt));
+  h.k = take(n * elem_size(dt));
+  h.v = take(n * elem_size(dt));
+  h.out = take(n * 4);
+  h.lse = take(static_cast<size_t>(B) * H * S * 4);
+  h.ws_bytes = ws_layout(B, H, S, D, R, U, dt, mode).total;
+  h.ws = take(h.ws_bytes);
+  h.total = o;
+  return h;
+}
+
+}  // extern "C" (reopened below)
+
+static cp_status host_pipe(int dev, HostPipe** out) {
+  HostPipe& p = g_pipe[dev];
+  if (!p.ready) {
+    if (cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.out_done, cudaEventDisableTiming) != cudaSuccess)
+      return CP_ERR_CUDA;
+    for (int j = 0; j < kMaxHostChunks; ++j)
+      if (cudaEventCreateWithFlags(&p.in_done[j], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&p.comp_done[j], cudaEventDisableTiming) != cudaSuccess)
+        return CP_ERR_CUDA;
+    p.ready = true;
+  }
+  *out = &p;
+  return CP_OK;
+}
+
+extern "C" {
+
+size_t cp_attention_host_buffer_size(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt,
+                                     cp_lap_mode mode) {
+  if (B < 0 || H < 1 || S < 0 || D < 1 || ring_degree < 1 || ulysses_degree < 1) return 0;
+  return host_layout(B, H, S, D, ring_degree, ulysses_degree, dt, mode).total;
+}
+
+cp_status cp_attention_fwd_host(const void* q, const void* k, const void* v, float* out, float* lse, int B, int H,
+                                int S, int D, float scale, int ring_degree, int ulysses_degree, int uneven_ok,
+                                void* dev_buffer, size_t dev_bytes, cp_dtype dt, cp_lap_mode mode, int head_chunks,
+                                void* stream) {
+  cp_status st = cp_attention_validate(B, H, S, D, ring_degree, ulysses_degree, uneven_ok, dt);
+  if (st != CP_OK) return st;
+  if (!std::isfinite(scale) || (mode != CP_LAP_FUSED && mode != CP_LAP_STEPWISE) || head_chunks < 1)
+    return CP_ERR_INVALID_ARG;
+  if (B == 0 || S == 0) return CP_OK;
+  if (!q || !k || !v || !out || !lse || !dev_buffer) return CP_ERR_INVALID_ARG;
+  const int R = ring_degree, U = ulysses_degree;
+  const HostLayout L = host_layout(B, H, S, D, R, U, dt, mode);
+  if (dev_bytes < L.total) return CP_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(dev_buffer) & 255) return CP_ERR_ALIGNMENT;
+  DeviceInfo* dinfo = nullptr;
+  if ((st = current_device(&dinfo)) != CP_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(dev_buffer);
+  const int eb = elem_size(dt);
+  const size_t n = static_cast<size_t>(B) * S * H * D;
+  void* dq = base + L.q;
+  void* dk = base + L.k;
+  void* dv = base + L.v;
+  float* dout = reinterpret_cast<float*>(base + L.out);
+  float* dlse = reinterpret_cast<float*>(base + L.lse);
+  // chunks of heads only where heads are independent launches: a fused lap
+  // (or plain attention) without Ulysses regroups
+  int chunks = head_chunks < H ? head_chunks : H;
+  if (chunks > kMaxHostChunks) chunks = kMaxHostChunks;
+  if (U > 1 || (mode == CP_LAP_STEPWISE && R > 1)) chunks = 1;
+  if (chunks == 1) {
+    if (cudaMemcpyAsync(dq, q, n * eb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dk, k, n * eb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dv, v, n * eb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return CP_ERR_CUDA;
+    if ((st = cp_attention_fwd(dq, dk, dv, dout, dlse, B, H, S, D, scale, R, U, uneven_ok, base + L.ws, L.ws_bytes,
+                               dt, mode, stream)) != CP_OK)
+      return st;
+    if (cudaMemcpyAsync(out, dout, n * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(lse, dlse, static_cast<size_t>(B) * H * S * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return CP_ERR_CUDA;
+    return CP_OK;
+  }
+  HostPipe* p = nullptr;
+  std::lock_guard<std::mutex> lk(g_pipe[dev].mu);
+  if ((st = host_pipe(dev, &p)) != CP_OK) return st;
+  int off[cp::kMaxRanks], len[cp::kMaxRanks];
+  if ((st = shard_table(S, R, uneven_ok != 0, off, len)) != CP_OK) return st;
+  RingGeom g;
+  fill_geom(&g, dt, R, off, len, R, off, len, -1);
+  std::vector<int> ho(chunks), hl(chunks);
+  if (shard_table(H, chunks, true, ho.data(), hl.data()) != CP_OK) return CP_ERR_INVALID_ARG;
+  const size_t row_b = static_cast<size_t>(H) * D * eb, row4 = static_cast<size_t>(H) * D * 4;
+  // copies start after everything already queued on the caller's stream
+  if (cudaEventRecord(p->start, s) != cudaSuccess || cudaStreamWaitEvent(p->in, p->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->out, p->start, 0) != cudaSuccess)
+    return CP_ERR_CUDA;
+  for (int j = 0; j < chunks; ++j) {
+    const size_t hb = static_cast<size_t>(ho[j]) * D;  // element offset of the chunk's first head
+    const size_t w_b = static_cast<size_t>(hl[j]) * D * eb, w4 = static_cast<size_t>(hl[j]) * D * 4;
+    const void* src[3] = {q, k, v};
+    void* dst[3] = {dq, dk, dv};
+    for (int i = 0; i < 3; ++i)
+      if (cudaMemcpy2DAsync(static_cast<char*>(dst[i]) + hb * eb, row_b, static_cast<const char*>(src[i]) + hb * eb,
+                            row_b, w_b, static_cast<size_t>(B) * S, cudaMemcpyHostToDevice, p->in) != cudaSuccess)
+        return CP_ERR_CUDA;
+    if (cudaEventRecord(p->in_done[j], p->in) != cudaSuccess || cudaStreamWaitEvent(s, p->in_done[j], 0) != cudaSuccess)
+      return CP_ERR_CUDA;
+    AttnTensors t{static_cast<const char*>(dq) + hb * eb, static_cast<const char*>(dk) + hb * eb,
+                  static_cast<const char*>(dv) + hb * eb, B, hl[j], D, S, S,
+                  static_cast<int64_t>(S) * H * D, static_cast<int64_t>(S) * H * D, dout + hb,
+                  static_cast<int64_t>(S) * H * D, dlse + static_cast<size_t>(ho[j]) * S};
+    t.row = static_cast<int64_t>(H) * D;
+    t.l_bstride = static_cast<int64_t>(H) * S;
+    if ((st = launch_attention(t, g, scale, dt, dinfo, s)) != CP_OK) return st;
+    if (cudaEventRecord(p->comp_done[j], s) != cudaSuccess || cudaStreamWaitEvent(p->out, p->comp_done[j], 0) != cudaSuccess)
+      return CP_ERR_CUDA;
+    if (cudaMemcpy2DAsync(reinterpret_cast<char*>(out) + hb * 4, row4, reinterpret_cast<const char*>(dout + hb), row4,
+                          w4, static_cast<size_t>(B) * S, cudaMemcpyDeviceToHost, p->out) != cudaSuccess ||
+        cudaMemcpy2DAsync(reinterpret_cast<char*>(lse) + static_cast<size_t>(ho[j]) * S * 4,
+                          static_cast<size_t>(H) * S * 4,
+                          reinterpret_cast<const char*>(dlse + static_cast<size_t>(ho[j]) * S),
+                          static_cast<size_t>(H) * S * 4, static_cast<size_t>(hl[j]) * S * 4, static_cast<size_t>(B),
+                          cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
+      return CP_ERR_CUDA;
+  }
+  // the caller's stream resumes once every result is back in host memory
+  if (cudaEventRecord(p->out_done, p->out) != cudaSuccess || cudaStreamWaitEvent(s, p->out_done, 0) != cudaSuccess)
+    return CP_ERR_CUDA;
   return CP_OK;
 }
 

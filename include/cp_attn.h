@@ -222,6 +222,36 @@ cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* o
                            void* stream);
 
 /*
+ * cp_attention_fwd over HOST buffers: q, k, v, out, lse as in
+ * cp_attention_fwd but in host memory (page-locked for the copies to overlap;
+ * pageable memory works, without overlap). dev_buffer (device, 256-byte
+ * aligned, caller-owned) must hold cp_attention_host_buffer_size(...) bytes:
+ * device copies of q, k, v, out, lse and the workspace of cp_attention_fwd.
+ * With ulysses_degree == 1 and the fused lap (or ring_degree == 1), the
+ * heads are split into head_chunks balanced ranges (at most 16): chunk j's
+ * q, k, v are copied in on a library copy stream while chunk j-1 computes on
+ * `stream`, and its out, lse are copied back on a second library copy stream
+ * while later chunks compute, so the transfers overlap each other and the
+ * attention. Heads are independent, so the result equals cp_attention_fwd's
+ * on the same inputs bit for bit. Otherwise (Ulysses regroups, or a stepwise
+ * ring lap) everything runs in order on `stream` (head_chunks is ignored).
+ * All work is ordered after the work already queued on `stream`, and `stream`
+ * resumes only after out and lse are in host memory; the call returns without
+ * waiting. The host buffers must stay valid and unchanged until then. Calls on
+ * one device serialise their enqueueing (the copy streams and their events
+ * are the library's, one set per device). Errors: those of cp_attention_fwd,
+ * INVALID_ARG for head_chunks < 1 or a null pointer, WORKSPACE when
+ * dev_bytes is too small.
+ */
+size_t cp_attention_host_buffer_size(int B, int H, int S, int D, int ring_degree, int ulysses_degree,
+                                     cp_dtype dt, cp_lap_mode mode);
+cp_status cp_attention_fwd_host(const void* q, const void* k, const void* v, float* out, float* lse,
+                                int B, int H, int S, int D, float scale,
+                                int ring_degree, int ulysses_degree, int uneven_ok,
+                                void* dev_buffer, size_t dev_bytes, cp_dtype dt, cp_lap_mode mode,
+                                int head_chunks, void* stream);
+
+/*
  * Synchronizes stream, then reads and clears the device error word on the
  * current device. Returns CP_OK if no kernel reported an expired wait since
  * the last call, CP_ERR_TIMEOUT if one did, CP_ERR_CUDA if the read failed.

@@ -354,6 +354,27 @@ def test_softmax_rescale_branches(case, mode):
     assert cpa().cp_check_device_status() == 0
 
 
+@pytest.mark.parametrize("name,mode,chunks", [
+    ("flux_ring4", "fused", 1), ("flux_ring4", "fused", 3), ("flux_ring4", "fused", 4),
+    ("ring_anything3", "fused", 5), ("flux_ulysses4", "fused", 4), ("tiny_ring", "fused", 2),
+    ("flux_ring4", "stepwise", 4),
+])
+def test_attention_fwd_host_equals_device_call(name, mode, chunks):
+    """The host-buffer entry point (copies overlapping compute over head chunks) gives the device
+    entry point's result bit for bit: heads are independent launches of the same kernel."""
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed, w.q_mult)
+    ref_out, ref_lse = run_fwd(*dev(q, k, v), w, mode)
+    qp, kp, vp = (t.pin_memory() for t in (q, k, v))
+    out = torch.full((w.B, w.S, w.H, w.D), float("nan")).pin_memory()
+    lse = torch.full((w.B, w.H, w.S), float("nan")).pin_memory()
+    cpa().cp_attention_fwd_host(qp, kp, vp, out, lse, w.scale, w.ring_degree, w.ulysses_degree, w.uneven_ok,
+                                mode=mode, head_chunks=chunks)
+    torch.cuda.synchronize()
+    assert cpa().cp_check_device_status() == 0
+    assert torch.equal(out, ref_out.cpu()) and torch.equal(lse, ref_lse.cpu())
+
+
 def test_cp_attention_modes_agree_and_deterministic():
     w = WORKLOADS["flux_ring4"]
     q, k, v = dev(*make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed))
