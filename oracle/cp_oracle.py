@@ -46,7 +46,7 @@ def _f64(x) -> np.ndarray:
 # Reading R3: non-causal, no mask, no dropout ([CP] Ring Anything note:
 # inference only, attn_mask must be None).
 # ---------------------------------------------------------------------------
-def attention(q, k, v, scale: float, row_chunk: int = 1024):
+def attention(q, k, v, scale: float, row_chunk: int = 1024, key_mask=None):
     """Softmax attention of q against one K/V block, returning (out, lse).
 
     For each batch b, head h and query row i:
@@ -57,6 +57,11 @@ def attention(q, k, v, scale: float, row_chunk: int = 1024):
         lse    = m_i + ln(l_i)
     An empty block (Skv = 0) gives out = 0 and lse = -inf (reading R6), the
     identity element of ``lse_merge``.
+
+    key_mask: None, or a boolean [B, Skv] array; keys where it is False take
+    no part (reading R17: a key-padding mask, the attn_mask the pages rule
+    out only for Ring Anything). Here they are simply left out of the sums;
+    a batch entry with no key left gets out = 0, lse = -inf (as R6).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Sq, H, D = q.shape
@@ -66,10 +71,16 @@ def attention(q, k, v, scale: float, row_chunk: int = 1024):
     lse = np.full((B, H, Sq), NEG_INF, dtype=np.float64)
     if Skv == 0 or Sq == 0:
         return out, lse
+    if key_mask is not None:
+        key_mask = np.asarray(key_mask, dtype=bool)
+        assert key_mask.shape == (B, Skv)
     for b in range(B):
+        keep = slice(None) if key_mask is None else np.nonzero(key_mask[b])[0]
+        if key_mask is not None and len(keep) == 0:
+            continue
         for h in range(H):
-            kt = k[b, :, h, :].T
-            vb = v[b, :, h, :]
+            kt = k[b, keep, h, :].T
+            vb = v[b, keep, h, :]
             for i0 in range(0, Sq, row_chunk):
                 i1 = min(Sq, i0 + row_chunk)
                 s = scale * (q[b, i0:i1, h, :] @ kt)
@@ -81,10 +92,10 @@ def attention(q, k, v, scale: float, row_chunk: int = 1024):
     return out, lse
 
 
-def attention_rows(q, k, v, scale: float, rows):
+def attention_rows(q, k, v, scale: float, rows, key_mask=None):
     """``attention`` for selected query rows only (rows are independent)."""
     q = _f64(q)
-    return attention(q[:, np.asarray(rows)], k, v, scale)
+    return attention(q[:, np.asarray(rows)], k, v, scale, key_mask=key_mask)
 
 
 # ---------------------------------------------------------------------------
@@ -144,26 +155,28 @@ def ring_shard_table(S: int, n: int, uneven_ok: bool):
 # block of rank (r - t) mod N (it receives from its predecessor, own block
 # first). The accumulator starts as the t = 0 partial.
 # ---------------------------------------------------------------------------
-def _ring_lap_rows(q_r, k, v, scale, table, r):
+def _ring_lap_rows(q_r, k, v, scale, table, r, key_mask=None):
     n = len(table)
     acc = None
     for t in range(n):
         j = (r - t) % n
         off, ln = table[j]
-        part = attention(q_r, k[:, off:off + ln], v[:, off:off + ln], scale)
+        km = None if key_mask is None else key_mask[:, off:off + ln]
+        part = attention(q_r, k[:, off:off + ln], v[:, off:off + ln], scale, key_mask=km)
         acc = part if acc is None else lse_merge(acc[0], acc[1], part[0], part[1])
     return acc
 
 
-def ring_attention(q, k, v, scale: float, ring_degree: int, uneven_ok: bool = False):
-    """Simulated ring lap over ``ring_degree`` ranks; returns global (out, lse)."""
+def ring_attention(q, k, v, scale: float, ring_degree: int, uneven_ok: bool = False, key_mask=None):
+    """Simulated ring lap over ``ring_degree`` ranks; returns global (out, lse).
+    A key mask travels with its K/V block (each block's slice of it)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, S, H, D = q.shape
     table = ring_shard_table(S, ring_degree, uneven_ok)
     out = np.zeros((B, S, H, D))
     lse = np.full((B, H, S), NEG_INF)
     for r, (off, ln) in enumerate(table):
-        o_r, l_r = _ring_lap_rows(q[:, off:off + ln], k, v, scale, table, r)
+        o_r, l_r = _ring_lap_rows(q[:, off:off + ln], k, v, scale, table, r, key_mask)
         out[:, off:off + ln] = o_r
         lse[:, :, off:off + ln] = l_r
     return out, lse
@@ -226,8 +239,9 @@ def _split_seq(x, n):
     return np.stack([x[:, u * Sl:(u + 1) * Sl] for u in range(n)])
 
 
-def ulysses_attention(q, k, v, scale: float, ulysses_degree: int):
-    """All-to-all, attention over all tokens of a head group, inverse all-to-all."""
+def ulysses_attention(q, k, v, scale: float, ulysses_degree: int, key_mask=None):
+    """All-to-all, attention over all tokens of a head group, inverse all-to-all.
+    A key mask indexes tokens, which every head group holds in full."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, S, H, D = q.shape
     U = ulysses_degree
@@ -236,7 +250,7 @@ def ulysses_attention(q, k, v, scale: float, ulysses_degree: int):
     qh, kh, vh = (seq2head(_split_seq(t, U)) for t in (q, k, v))
     outs, lses = [], []
     for g in range(U):
-        o, l = attention(qh[g], kh[g], vh[g], scale)
+        o, l = attention(qh[g], kh[g], vh[g], scale, key_mask=key_mask)
         outs.append(o)
         lses.append(l)
     out = np.concatenate(list(head2seq(np.stack(outs))), axis=1)
@@ -308,7 +322,7 @@ def anything_head2seq_lse(lse_groups):
     return out
 
 
-def ulysses_anything_attention(q, k, v, scale: float, ulysses_degree: int):
+def ulysses_anything_attention(q, k, v, scale: float, ulysses_degree: int, key_mask=None):
     """Ulysses with balanced, possibly uneven token shards and head groups."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, S, H, D = q.shape
@@ -319,7 +333,7 @@ def ulysses_anything_attention(q, k, v, scale: float, ulysses_degree: int):
     qh, kh, vh = (anything_seq2head([t[:, so:so + sl] for so, sl in seq]) for t in (q, k, v))
     outs, lses = [], []
     for g in range(U):
-        o, l = attention(qh[g], kh[g], vh[g], scale)
+        o, l = attention(qh[g], kh[g], vh[g], scale, key_mask=key_mask)
         outs.append(o)
         lses.append(l)
     out = np.concatenate(anything_head2seq(outs), axis=1)
@@ -336,7 +350,7 @@ def ulysses_anything_attention(q, k, v, scale: float, ulysses_degree: int):
 # group r is ring row r, which after its regroup holds tokens
 # [r*S/R, (r+1)*S/R) for head group u.
 # ---------------------------------------------------------------------------
-def unified_attention(q, k, v, scale: float, ring_degree: int, ulysses_degree: int):
+def unified_attention(q, k, v, scale: float, ring_degree: int, ulysses_degree: int, key_mask=None):
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, S, H, D = q.shape
     R, U = ring_degree, ulysses_degree
@@ -356,7 +370,8 @@ def unified_attention(q, k, v, scale: float, ring_degree: int, ulysses_degree: i
             acc = None
             for t in range(R):
                 j = (r - t) % R
-                part = attention(rows[r][0][g], rows[j][1][g], rows[j][2][g], scale)
+                km = None if key_mask is None else key_mask[:, j * Sr:(j + 1) * Sr]
+                part = attention(rows[r][0][g], rows[j][1][g], rows[j][2][g], scale, key_mask=km)
                 acc = part if acc is None else lse_merge(acc[0], acc[1], part[0], part[1])
             outs.append(acc[0])
             lses.append(acc[1])
@@ -366,13 +381,15 @@ def unified_attention(q, k, v, scale: float, ring_degree: int, ulysses_degree: i
 
 
 def cp_attention(q, k, v, scale: float, ring_degree: int = 1, ulysses_degree: int = 1,
-                 uneven_ok: bool = False):
+                 uneven_ok: bool = False, key_mask=None):
     """Dispatch on the ContextParallelConfig degrees ([CP] variants table).
 
     Ring (ring_degree > 1), Ulysses (ulysses_degree > 1), Unified (both > 1).
     uneven_ok selects an Anything variant: Ring Anything (ring_degree > 1,
     ulysses_degree == 1) or Ulysses Anything (ulysses_degree > 1,
     ring_degree == 1); neither combines with the other degree.
+    key_mask: optional boolean [B, S] key-padding mask (R17); Ring Anything
+    takes none ([CP] Ring Anything Attention: attn_mask must be None).
     """
     q = _f64(q)
     B, S, H, D = q.shape
@@ -381,12 +398,16 @@ def cp_attention(q, k, v, scale: float, ring_degree: int = 1, ulysses_degree: in
         raise ValueError("degrees must be >= 1")
     if uneven_ok and (R > 1) == (U > 1):
         raise UnsupportedComboError("an Anything variant needs exactly one of ring_degree, ulysses_degree > 1")
+    if uneven_ok and R > 1 and key_mask is not None:
+        raise UnsupportedComboError("Ring Anything takes no attention mask")
+    if key_mask is not None:
+        key_mask = np.asarray(key_mask, dtype=bool)
     if U > H:
         raise ValueError(f"ulysses_degree {U} exceeds the number of heads {H}")
     if uneven_ok and U > 1:
-        return ulysses_anything_attention(q, k, v, scale, U)
+        return ulysses_anything_attention(q, k, v, scale, U, key_mask)
     if U == 1:
-        return ring_attention(q, k, v, scale, R, uneven_ok)
+        return ring_attention(q, k, v, scale, R, uneven_ok, key_mask)
     if R == 1:
-        return ulysses_attention(q, k, v, scale, U)
-    return unified_attention(q, k, v, scale, R, U)
+        return ulysses_attention(q, k, v, scale, U, key_mask)
+    return unified_attention(q, k, v, scale, R, U, key_mask)

@@ -494,3 +494,81 @@ def test_planted_anything_mistakes_are_caught(kind):
     right = co.anything_seq2head([x[:, _bal_off(S, U, u):_bal_off(S, U, u + 1)] for u in range(U)])
     assert any(w.shape != r.shape or not np.array_equal(w, r) for w, r in zip(wrong, right)) or \
         [cut[u + 1] - cut[u] for u in range(U)] != [_bal_off(S, U, u + 1) - _bal_off(S, U, u) for u in range(U)]
+
+
+# ---------------------------------------------------------------------------
+# Key-padding mask (reading R17): masked keys take no part in the softmax.
+# ---------------------------------------------------------------------------
+def _brute_masked(q, k, v, scale, km):
+    """Scalar loops with math.fsum, masked keys skipped; no max shift."""
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    out = np.zeros((B, Sq, H, D))
+    lse = np.full((B, H, Sq), -np.inf)
+    for b in range(B):
+        for h in range(H):
+            for i in range(Sq):
+                keys = [j for j in range(Skv) if km[b, j]]
+                if not keys:
+                    continue
+                e = [math.exp(scale * math.fsum(q[b, i, h, d] * k[b, j, h, d] for d in range(D))) for j in keys]
+                z = math.fsum(e)
+                for d in range(D):
+                    out[b, i, h, d] = math.fsum(e[t] * v[b, j, h, d] for t, j in enumerate(keys)) / z
+                lse[b, h, i] = math.log(z)
+    return out, lse
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_masked_attention_matches_brute_force(seed):
+    B, Sq, Skv, H, D = 2, 3, 7, 2, 3
+    q, k, v = (rnd((B, n, H, D), seed + 10 * i) for i, n in enumerate((Sq, Skv, Skv)))
+    km = np.random.default_rng(seed).random((B, Skv)) < 0.6
+    km[1, :] = False if seed == 2 else km[1, :]  # seed 2: a batch entry with every key masked
+    o, l = oracle.attention(q, k, v, 0.7, key_mask=km)
+    bo, bl = _brute_masked(q, k, v, 0.7, km)
+    assert np.array_equal(np.isneginf(l), np.isneginf(bl))
+    fin = np.isfinite(bl)
+    assert np.max(np.abs(o - bo)) <= 1e-13 and np.max(np.abs(l[fin] - bl[fin])) <= 1e-13
+    if seed == 2:
+        assert np.all(o[1] == 0) and np.all(np.isneginf(l[1]))
+
+
+def test_mask_all_true_is_no_mask_and_single_key_closed_form():
+    q, k, v = (rnd((2, 5, 3, 4), i) for i in range(3))
+    o0, l0 = oracle.attention(q, k, v, 0.5)
+    o1, l1 = oracle.attention(q, k, v, 0.5, key_mask=np.ones((2, 5), bool))
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    km = np.zeros((2, 5), bool)
+    km[:, 3] = True  # one key left: out = v_3, lse = its logit
+    o, l = oracle.attention(q, k, v, 0.5, key_mask=km)
+    assert np.allclose(o, np.broadcast_to(v[:, 3:4], o.shape), atol=1e-15)
+    assert np.allclose(l, 0.5 * np.einsum("bihd,bhd->bhi", q, k[:, 3]), atol=1e-14)
+
+
+@pytest.mark.parametrize("R,U,ev,S,H", [(4, 1, False, 24, 2), (1, 4, False, 24, 8), (2, 2, False, 24, 4),
+                                        (1, 3, True, 23, 5), (3, 1, False, 24, 2)])
+def test_masked_decompositions_equal_masked_attention(R, U, ev, S, H):
+    q, k, v = (rnd((2, S, H, 3), 40 + i) for i in range(3))
+    km = np.random.default_rng(S + R).random((2, S)) < 0.5
+    km[0, : S // 2] = False  # whole ring blocks masked for entry 0
+    o, l = oracle.cp_attention(q, k, v, 0.3, R, U, ev, key_mask=km)
+    ro, rl = oracle.attention(q, k, v, 0.3, key_mask=km)
+    assert np.array_equal(np.isneginf(l), np.isneginf(rl))
+    fin = np.isfinite(rl)
+    assert np.max(np.abs(o - ro)) <= 1e-12 and np.max(np.abs(l[fin] - rl[fin])) <= 1e-12
+
+
+def test_mask_with_ring_anything_is_rejected():
+    q = rnd((1, 23, 2, 2), 0)
+    with pytest.raises(oracle.UnsupportedComboError):
+        oracle.cp_attention(q, q, q, 1.0, 3, 1, True, key_mask=np.ones((1, 23), bool))
+
+
+def test_planted_mask_on_queries_is_caught():
+    q, k, v = (rnd((1, 6, 2, 3), 50 + i) for i in range(3))
+    km = np.array([[True, False, True, True, False, True]])
+    o, l = oracle.attention(q, k, v, 0.6, key_mask=km)
+    # the mistake: drop the masked positions from the queries instead of the keys
+    wrong = oracle.attention(q, k, v, 0.6)[0] * km[:, :, None, None]
+    assert np.max(np.abs(wrong - o)) > 1e-3
