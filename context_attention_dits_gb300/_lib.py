@@ -48,6 +48,8 @@ SIGNATURES = {
     "cp_debug_bounded_wait_probe": (_i, [_i, _vp]),
     "cp_attention_fwd_no_alloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _i, _i, _vp]),
     "cp_attention_host_buffer_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
+    "cp_attention_fwd_masked": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz, _i, _i,
+                                     _vp]),
     "cp_attention_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz, _i, _i, _i,
                                    _vp]),
 }

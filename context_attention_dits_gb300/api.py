@@ -151,11 +151,13 @@ def cp_attention_launch_count(B, H, S, D, ring_degree=1, ulysses_degree=1, dtype
 
 
 def cp_attention_fwd(q, k, v, out, lse, scale: float, ring_degree: int = 1, ulysses_degree: int = 1,
-                     uneven_ok: bool = False, workspace=None, mode="fused", stream=None):
+                     uneven_ok: bool = False, workspace=None, mode="fused", stream=None, key_mask=None):
     """Context-parallel attention over global q, k, v [B,S,H,D] -> out [B,S,H,D] f32, lse [B,H,S] f32.
 
     workspace: a CUDA uint8 tensor of at least cp_attention_workspace_size(...)
-    bytes; allocated here through torch when None.
+    bytes; allocated here through torch when None. key_mask: optional CUDA
+    bool/uint8 tensor [B, S] (True/nonzero = the key takes part); calls
+    cp_attention_fwd_masked.
     """
     _cuda(q, k, v, out, lse)
     B, S, H, D = q.shape
@@ -172,6 +174,16 @@ def cp_attention_fwd(q, k, v, out, lse, scale: float, ring_degree: int = 1, ulys
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if key_mask is not None:
+        _cuda(key_mask)
+        if key_mask.shape != (B, S) or key_mask.dtype not in (torch.bool, torch.uint8) or not key_mask.is_contiguous():
+            raise ValueError("key_mask must be a dense bool or uint8 tensor [B, S]")
+        st = lib().cp_attention_fwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), key_mask.data_ptr(),
+                                           out.data_ptr(), lse.data_ptr(), B, H, S, D, float(scale), ring_degree,
+                                           ulysses_degree, int(bool(uneven_ok)), ws_ptr, ws_bytes, _dt(q), m,
+                                           _stream(stream))
+        check(st, "cp_attention_fwd_masked")
+        return
     st = lib().cp_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                                 B, H, S, D, float(scale), ring_degree, ulysses_degree, int(bool(uneven_ok)),
                                 ws_ptr, ws_bytes, _dt(q), m, _stream(stream))

@@ -137,7 +137,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D>
+template <int D, bool kMasked>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const __grid_constant__ AttnArgs a) {
@@ -398,7 +398,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       KvCursor cur;
       cur.init(a.g, r);
+      const uint8_t* km = kMasked ? a.kmask + (b % a.km_bmod) * a.km_bstride : nullptr;
       for (int it = 0; it < NT; ++it) {
+        // key mask of this tile as four 32-bit words: bit l of word j is key
+        // kv0 + 4l + j (read before the wait, so its latency overlaps it)
+        uint32_t kmw[4] = {~0u, ~0u, ~0u, ~0u};
+        if constexpr (kMasked) {
+          const int kv0 = cur.kv0(), nvk = cur.nvalid();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = 4 * lane + j;
+            kmw[j] = __ballot_sync(0xffffffffu, c < nvk && km[kv0 + c] != 0);
+          }
+        }
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarSFull + i), it & 1, abort_flag, a.err, tmo));
         if (!ok) break;
         tc_fence_after();
@@ -411,6 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kTileN; ++c)
             if (c >= nv) sr[c] = __float_as_uint(-INFINITY);
+        }
+        const bool tile_masked = kMasked && (kmw[0] & kmw[1] & kmw[2] & kmw[3]) != ~0u;  // uniform in the warp
+        if (tile_masked) {
+#pragma unroll
+          for (int c = 0; c < kTileN; ++c)
+            if (!((kmw[c & 3] >> (c >> 2)) & 1u)) sr[c] = __float_as_uint(-INFINITY);
         }
         // P = 2^(s*scale*log2e - m_used) rounded to bf16, packed in pairs into
         // pk; returns the row sum of the rounded P (the values the PV product
@@ -450,12 +468,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kTileN; ++c)
               if (c >= nv) sr[c] = __float_as_uint(-INFINITY);
           }
+          if (tile_masked) {
+#pragma unroll
+            for (int c = 0; c < kTileN; ++c)
+              if (!((kmw[c & 3] >> (c >> 2)) & 1u)) sr[c] = __float_as_uint(-INFINITY);
+          }
         };
         float f = 1.f, lsum;
-        if (it == 0) {
-          // no running maximum yet: the row maximum first
+        if (it == 0 || (kMasked && m_used == -INFINITY)) {
+          // no running maximum yet (first tile, or every key so far masked,
+          // which holds for every row alike): the row maximum first; a row
+          // with every key of the tile masked keeps -inf and P = 0
           m_used = row_max();
-          lsum = exp_pass(-m_used);
+          lsum = exp_pass(m_used == -INFINITY ? 0.f : -m_used);
         } else {
           // speculatively with the running maximum. Every P is at most the
           // row sum, so a row sum within 2^8 proves that the row maximum is
@@ -502,8 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int rows_valid = rows[i];
         const int tok0 = qrow[i];  // first token of this tile
-        const float inv_l = NT > 0 ? 1.f / l : 0.f;
-        const float lse_v = NT > 0 ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        // l = 0: no key (an empty lap, or every key masked) -> out 0, lse -inf
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const float lse_v = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
         if (row < rows_valid) a.lse[b * a.l_bstride + h * a.l_hstride + tok0 + row] = lse_v;
         // all of O's row from TMEM at once, then per 32-column chunk: stage 32
         // rows x 32 fp32 per warp in this tile's (now idle) Q buffer, 128B-
@@ -579,7 +605,9 @@ cudaError_t launch_tc_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensor
                         cudaStream_t s) {
   using L = Smem<D>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  // the key-mask code is compiled only into the masked instance
+  auto kernel = a.kmask ? attn_fwd_tc_kernel<D, true> : attn_fwd_tc_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   // two-tile items (pairs, plus leftover tiles paired across shards over a
   // whole lap) and one-tile items; see the work-item decode in the kernel
@@ -588,7 +616,7 @@ cudaError_t launch_tc_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensor
   const int64_t items = static_cast<int64_t>(a.g.pair_prefix[a.g.n_q] + n_single - n_cross) * a.H * a.B;
   if (items == 0) return cudaSuccess;
   if (items > 0x7fffffff) return cudaErrorInvalidValue;
-  attn_fwd_tc_kernel<D><<<dim3(static_cast<unsigned>(items)), kThreads, L::kAlloc, s>>>(tq, tk, tv, a);
+  kernel<<<dim3(static_cast<unsigned>(items)), kThreads, L::kAlloc, s>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 

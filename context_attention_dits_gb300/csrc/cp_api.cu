@@ -147,6 +147,9 @@ struct AttnTensors {
   int hv_short_from = INT_MAX;     // first group whose last head is padding
   int64_t row = 0;                 // token stride of q, k, v and out in elements (0: H*D)
   int64_t l_bstride = 0;           // batch stride of lse in elements (0: H*Sq)
+  const uint8_t* kmask = nullptr;  // key-padding mask [km_bmod, km_bstride] (nullptr: none)
+  int64_t km_bstride = 0;
+  int km_bmod = 1;
 };
 
 cp_status launch_attention(const AttnTensors& t, const RingGeom& g, float scale, cp_dtype dt, DeviceInfo* dev,
@@ -170,6 +173,9 @@ cp_status launch_attention(const AttnTensors& t, const RingGeom& g, float scale,
   a.timeout_ns = kWaitTimeoutNs;
   a.hv_bpg = t.hv_bpg;
   a.hv_short_from = t.hv_short_from;
+  a.kmask = t.kmask;
+  a.km_bstride = t.km_bstride;
+  a.km_bmod = t.km_bmod > 0 ? t.km_bmod : 1;
   cudaError_t e;
   if (dt == CP_BF16) {
     CUtensorMap tq, tk, tv;
@@ -423,9 +429,13 @@ int cp_attention_launch_count(int B, int H, int S, int D, int ring_degree, int u
   return n;
 }
 
-cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* out, float* lse, int B, int H, int S,
-                           int D, float scale, int ring_degree, int ulysses_degree, int uneven_ok, void* workspace,
-                           size_t ws_bytes, cp_dtype dt, cp_lap_mode mode, void* stream) {
+}  // extern "C" (reopened below)
+
+// cp_attention_fwd with an optional key-padding mask [B, S] (device, nonzero = attend).
+static cp_status attention_fwd_impl(const void* q, const void* k, const void* v, const uint8_t* key_mask, float* out,
+                                    float* lse, int B, int H, int S, int D, float scale, int ring_degree,
+                                    int ulysses_degree, int uneven_ok, void* workspace, size_t ws_bytes, cp_dtype dt,
+                                    cp_lap_mode mode, void* stream) {
   cp_status st = cp_attention_validate(B, H, S, D, ring_degree, ulysses_degree, uneven_ok, dt);
   if (st != CP_OK) return st;
   if (!std::isfinite(scale) || (mode != CP_LAP_FUSED && mode != CP_LAP_STEPWISE)) return CP_ERR_INVALID_ARG;
@@ -494,6 +504,9 @@ cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* o
       t.hv_bpg = B;
       t.hv_short_from = H % U;
     }
+    t.kmask = key_mask;  // batch entry (g, b) of a Ulysses group reads mask row b
+    t.km_bstride = S;
+    t.km_bmod = B;
     if ((st = launch_attention(t, g, scale, dt, dev, s)) != CP_OK) return st;
   } else {
     float* op = reinterpret_cast<float*>(ws + w.op);
@@ -502,6 +515,9 @@ cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* o
       RingGeom g;
       fill_geom(&g, dt, R, off, len, R, off, len, step);
       AttnTensors t{qa, ka, va, Bn, Hg, D, S, S, bstride, bstride, step == 0 ? oa : op, bstride, step == 0 ? la : lp};
+      t.kmask = key_mask;
+      t.km_bstride = S;
+      t.km_bmod = B;
       if ((st = launch_attention(t, g, scale, dt, dev, s)) != CP_OK) return st;
       if (step > 0 && cp::launch_lse_merge(oa, la, op, lp, Bn, Hg, S, D, s) != cudaSuccess) return CP_ERR_CUDA;
     }
@@ -527,6 +543,25 @@ cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* o
     }
   }
   return CP_OK;
+}
+
+extern "C" {
+
+cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* out, float* lse, int B, int H, int S,
+                           int D, float scale, int ring_degree, int ulysses_degree, int uneven_ok, void* workspace,
+                           size_t ws_bytes, cp_dtype dt, cp_lap_mode mode, void* stream) {
+  return attention_fwd_impl(q, k, v, nullptr, out, lse, B, H, S, D, scale, ring_degree, ulysses_degree, uneven_ok,
+                            workspace, ws_bytes, dt, mode, stream);
+}
+
+cp_status cp_attention_fwd_masked(const void* q, const void* k, const void* v, const uint8_t* key_mask, float* out,
+                                  float* lse, int B, int H, int S, int D, float scale, int ring_degree,
+                                  int ulysses_degree, int uneven_ok, void* workspace, size_t ws_bytes, cp_dtype dt,
+                                  cp_lap_mode mode, void* stream) {
+  // Ring Anything takes no mask ("Ring Anything Attention": attn_mask must be None)
+  if (key_mask && uneven_ok && ring_degree > 1) return CP_ERR_UNSUPPORTED_COMBO;
+  return attention_fwd_impl(q, k, v, key_mask, out, lse, B, H, S, D, scale, ring_degree, ulysses_degree, uneven_ok,
+                            workspace, ws_bytes, dt, mode, stream);
 }
 
 // ---------------------------------------------------------------------------

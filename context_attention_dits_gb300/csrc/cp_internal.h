@@ -56,6 +56,11 @@ struct AttnArgs {
   // is padding and is skipped). hv_bpg = 1, hv_short_from = INT_MAX: none.
   int hv_bpg;
   int hv_short_from;
+  // key-padding mask (nullptr: none): key j of batch entry b takes part iff
+  // kmask[(b % km_bmod) * km_bstride + j] != 0 (j indexes the K/V tokens)
+  const uint8_t* kmask;
+  int64_t km_bstride;
+  int km_bmod;
 };
 
 // Whether (head h, batch entry b) is padding of a ragged head group.

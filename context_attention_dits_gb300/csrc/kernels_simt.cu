@@ -48,7 +48,9 @@ __global__ void __launch_bounds__(32 * kF32RowsPerCta) attn_fwd_f32_kernel(const
     int j = (r - s) % a.g.n_kv;
     if (j < 0) j += a.g.n_kv;
     const int off = a.g.kv_off[j], len = a.g.kv_len[j];
+    const uint8_t* km = a.kmask ? a.kmask + (b % a.km_bmod) * a.km_bstride : nullptr;
     for (int key = off; key < off + len; ++key) {
+      if (km && km[key] == 0) continue;  // masked key: no part in the softmax
       const float* krow = a.kf + b * a.kv_bstride + key * a.kv_sstride + h * D;
       const float* vrow = a.vf + b * a.kv_bstride + key * a.kv_sstride + h * D;
       float part = 0.f;

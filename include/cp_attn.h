@@ -222,6 +222,25 @@ cp_status cp_attention_fwd(const void* q, const void* k, const void* v, float* o
                            void* stream);
 
 /*
+ * cp_attention_fwd with a key-padding mask: key_mask is a device array of B*S
+ * bytes, row-major [B, S]; key j of batch entry b takes part in the softmax
+ * of every query and head of that entry iff key_mask[b*S + j] != 0, and a
+ * query row whose keys are all masked gets out = 0, lse = -inf. The pages
+ * only say that Ring Anything takes no attention mask ("Paralelismo de
+ * contexto", Ring Anything Attention: attn_mask must be None); the mask form
+ * is this library's reading (a key-padding mask, as for padded text tokens).
+ * key_mask == NULL is exactly cp_attention_fwd. Every ring block, Ulysses
+ * head group and lap mode reads the mask at the global key position. Errors:
+ * those of cp_attention_fwd, plus UNSUPPORTED_COMBO for a mask with
+ * uneven_ok and ring_degree > 1 (Ring Anything).
+ */
+cp_status cp_attention_fwd_masked(const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                                  float* out, float* lse, int B, int H, int S, int D, float scale,
+                                  int ring_degree, int ulysses_degree, int uneven_ok,
+                                  void* workspace, size_t ws_bytes, cp_dtype dt, cp_lap_mode mode,
+                                  void* stream);
+
+/*
  * cp_attention_fwd over HOST buffers: q, k, v, out, lse as in
  * cp_attention_fwd but in host memory (page-locked for the copies to overlap;
  * pageable memory works, without overlap). dev_buffer (device, 256-byte

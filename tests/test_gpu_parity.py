@@ -375,6 +375,72 @@ def test_attention_fwd_host_equals_device_call(name, mode, chunks):
     assert torch.equal(out, ref_out.cpu()) and torch.equal(lse, ref_lse.cpu())
 
 
+# ----------------------------------------------------------------------------
+# key-padding mask (cp_attention_fwd_masked)
+# ----------------------------------------------------------------------------
+def run_fwd_masked(q, k, v, km, w, mode):
+    B, S, H, D = q.shape
+    out = torch.empty((B, S, H, D), device="cuda")
+    lse = torch.empty((B, H, S), device="cuda")
+    cpa().cp_attention_fwd(q, k, v, out, lse, w.scale, w.ring_degree, w.ulysses_degree, w.uneven_ok, mode=mode,
+                           key_mask=km.cuda())
+    torch.cuda.synchronize()
+    assert cpa().cp_check_device_status() == 0
+    return out, lse
+
+
+@pytest.mark.parametrize("mode", ["fused", "stepwise"])
+def test_masked_flux_text_padding(mode):
+    """FLUX ring 4 with the text part padded: keys 300..511 of the 512 text tokens masked."""
+    w = WORKLOADS["flux_ring4"]
+    q, k, v = make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed)
+    km = torch.ones((w.B, w.S), dtype=torch.bool)
+    km[:, 300:512] = False
+    ro, rl = oracle.cp_attention(q, k, v, w.scale, w.ring_degree, 1, False, key_mask=km.numpy())
+    out, lse = run_fwd_masked(*dev(q, k, v), km, w, mode)
+    check_attn(out, lse, ro, rl, BF16_TOL, f"masked flux/{mode}")
+
+
+@pytest.mark.parametrize("B,H,S,D,R,U,ev", [
+    (2, 4, 300, 64, 3, 1, False),     # ring 3 (100-token blocks)
+    (1, 8, 384, 128, 1, 4, False),    # Ulysses 4
+    (1, 8, 520, 128, 4, 2, False),    # unified 4 x 2
+    (2, 7, 300, 64, 1, 3, True),      # Ulysses Anything
+    (1, 4, 129, 128, 1, 1, False),    # plain attention
+])
+@pytest.mark.parametrize("mode", ["fused", "stepwise"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_masked_small_grid(B, H, S, D, R, U, ev, mode, dtype):
+    q, k, v = make_qkv(B, H, S, D, dtype, seed=S + 7 * R + U)
+    g = torch.Generator().manual_seed(S)
+    km = torch.rand((B, S), generator=g) < 0.6   # partly masked tiles everywhere
+    km[0, : S // 3] = False                      # a run of fully masked tiles / blocks
+    if B > 1:
+        km[1, :] = False                         # an entry with every key masked: out 0, lse -inf
+    class W:
+        pass
+    w = W()
+    w.scale, w.ring_degree, w.ulysses_degree, w.uneven_ok = D ** -0.5, R, U, ev
+    ro, rl = oracle.cp_attention(q, k, v, w.scale, R, U, ev, key_mask=km.numpy())
+    out, lse = run_fwd_masked(*dev(q, k, v), km, w, mode)
+    check_attn(out, lse, ro, rl, BF16_TOL if dtype == "bf16" else F32_TOL, f"masked grid {B},{H},{S},{D},{R},{U}")
+
+
+def test_mask_all_ones_is_bitwise_unmasked_and_ring_anything_rejects_a_mask():
+    w = WORKLOADS["ring_anything3"]
+    q, k, v = dev(*make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed))
+    km = torch.ones((w.B, w.S), dtype=torch.bool, device="cuda")
+    out = torch.empty((w.B, w.S, w.H, w.D), device="cuda")
+    lse = torch.empty((w.B, w.H, w.S), device="cuda")
+    with pytest.raises(cpa().CpError):
+        cpa().cp_attention_fwd(q, k, v, out, lse, w.scale, 3, 1, True, key_mask=km)
+    w4 = WORKLOADS["flux_ring4"]
+    q4, k4, v4 = dev(*make_qkv(w4.B, w4.H, w4.S, w4.D, w4.dtype, w4.seed))
+    ref = run_fwd(q4, k4, v4, w4, "fused")
+    got = run_fwd_masked(q4, k4, v4, torch.ones((w4.B, w4.S), dtype=torch.bool), w4, "fused")
+    assert torch.equal(ref[0], got[0]) and torch.equal(ref[1], got[1])
+
+
 def test_cp_attention_modes_agree_and_deterministic():
     w = WORKLOADS["flux_ring4"]
     q, k, v = dev(*make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed))
