@@ -235,6 +235,19 @@ def secondary(cpa, dev, flush, stream, peaks):
                      "launches": cpa.cp_attention_launch_count(w.B, w.H, w.S, w.D, w.ring_degree,
                                                                w.ulysses_degree, q.dtype, "fused")}
         del q, k, v, out, lse, ws
+    # key-padding mask: FLUX ring 4 with text keys 300..511 masked (FLOPs counted dense, as unmasked)
+    w = WORKLOADS["flux_ring4"]
+    q, k, v = (t.to(dev) for t in make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed, w.q_mult))
+    out = torch.empty((w.B, w.S, w.H, w.D), device=dev)
+    lse = torch.empty((w.B, w.H, w.S), device=dev)
+    km = torch.ones((w.B, w.S), dtype=torch.bool, device=dev)
+    km[:, 300:512] = False
+    ms = _time_events(lambda: cpa.cp_attention_fwd(q, k, v, out, lse, w.scale, w.ring_degree, 1, False,
+                                                    mode="fused", stream=stream, key_mask=km), flush, stream, 20)
+    tf = w.flops / (ms * 1e-3) / 1e12
+    res["flux_ring4_text_padding_mask"] = {"TFLOP_s": tf, "ms": ms, "frac_of_bf16_peak": tf / bf16, "launches": 1,
+                                           "note": "keys 300..511 masked; FLOPs counted as unmasked"}
+    del q, k, v, out, lse, km
     if cpa.cp_check_device_status() != 0:
         raise RuntimeError("device status after the secondary measurements")
     return res
