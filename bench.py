@@ -200,6 +200,15 @@ def secondary(cpa, dev, flush, stream, peaks):
        _time_batch(fns * 3, flush, stream, 5), "one rank-step merge; back_to_back: 24 merges over 8 operand sets")
     del sets, fns
 
+    # the same merge at the unified video step shape (R=2 x U=4, S=32768: one step's partial of all
+    # four head groups, [4, 32768, 6, 128] fp32, 402 MB), as the stepwise lap of that workload runs it
+    oa, la, ob, lb = (t.to(dev) for t in make_merge_operands(4, 6, 32768, 128, seed=9))
+    nbytes = 12 * oa.numel() + 12 * la.numel()
+    ms = _time_events(lambda: cpa.cp_lse_merge(oa, la, ob, lb, stream=stream), flush, stream, 10)
+    res["lse_merge_video_unified_step"] = {"bytes_per_launch": nbytes, "single_launch": {
+        "ms": ms, "GB_s": nbytes / ms / 1e6, "frac_of_hbm": nbytes / ms / 1e6 / hbm}}
+    del oa, la, ob, lb
+
     # Ulysses regroups of FLUX Ulysses-4: q, k, v (bf16) seq->head; out (fp32) head->seq
     U, S, H, D = 4, 4608, 24, 128
     xs = [torch.randn((U, 1, S // U, H, D), device=dev).to(torch.bfloat16) for _ in range(6)]
@@ -216,6 +225,17 @@ def secondary(cpa, dev, flush, stream, peaks):
     bw("head2seq_flux_ulysses4_f32", nbytes, _time_events(fns[0], flush, stream, 30),
        _time_batch(fns * 4, flush, stream, 5), "the fp32 output; back_to_back: 12 regroups over 3 tensor pairs")
     del xs, ys, fns
+    # a Ulysses-4 regroup at video length: q (bf16) 4 x [1, 8192, 24, 128] -> 4 x [1, 32768, 6, 128]
+    # (201 MB each way)
+    x = torch.randn((1, 32768, 24, 128), device=dev).to(torch.bfloat16)
+    y = torch.empty((4, 1, 32768, 6, 128), device=dev, dtype=torch.bfloat16)
+    xr = x.view(1, 4, 8192, 24, 128).permute(1, 0, 2, 3, 4).contiguous()  # four 8192-token rank shards
+    nbytes = 2 * x.numel() * 2
+    ms = _time_events(lambda: cpa.cp_ulysses_seq2head(xr.view(4, 1, 8192, 24, 128), y.view(4, 1, 32768, 6, 128),
+                                                       stream=stream), flush, stream, 10)
+    res["seq2head_32768tok_ulysses4_bf16"] = {"bytes_per_launch": nbytes, "single_launch": {
+        "ms": ms, "GB_s": nbytes / ms / 1e6, "frac_of_hbm": nbytes / ms / 1e6 / hbm}}
+    del x, y, xr
 
     # cp_attention_fwd on the other workloads (fused lap), inputs resident
     for name in ("flux_ulysses4", "ring_anything3", "video_unified", "flux1008_ulysses_anything4",
