@@ -15,9 +15,11 @@
 // API page, ContextParallelConfig.convert_to_fp32: fp32 output and LSE.)
 //
 // Warp roles (320 threads):
-//   warp 0        TMA producer: Q tiles once, then K and V tiles through a
-//                 two-stage ring each, 128B-swizzled.
-//   warp 1        TMEM allocator and MMA issuer (one thread):
+//   warp 0        TMA producer (the whole warp runs the loop, an elected lane
+//                 issues): Q tile 0, K(0), Q tile 1, then K and V tiles
+//                 through a two-stage ring each, 128B-swizzled.
+//   warp 1        TMEM allocator and MMA issuer (the whole warp runs the
+//                 loop, an elected lane issues and commits):
 //                 S_i = Q_i K^T (SS MMA, M=128 N=128 K=16 steps) and
 //                 O_i += P_i V (TS MMA, P read from TMEM), ping-ponging the
 //                 two query tiles so that one tile's softmax overlaps the
@@ -27,11 +29,17 @@
 //                 per query row (TMEM lane), row max and sum in registers,
 //                 P = 2^(s*scale*log2e - m) rounded to bf16 into TMEM over S
 //                 (l sums the rounded P, so out and lse are exact attention of
-//                 logits perturbed by at most one bf16 rounding of P),
-//                 O rescaled in TMEM only when the row max grows by more than
-//                 2^8 (the stale maximum is exact: it cancels in O / l).
+//                 logits perturbed by at most one bf16 rounding of P). After
+//                 the first tile P is computed with the running maximum and
+//                 the row sum checks it afterwards; O and l are rescaled only
+//                 when the row max grows by more than 2^8 (the stale maximum
+//                 is exact: it cancels in O / l).
 //                 Epilogue: O / l staged through shared memory and stored
 //                 coalesced; lse = (m + log2 l) * ln 2.
+// kMasked: the instance that also applies a key-padding mask, packed per K/V
+// tile by ballots of the tile's mask bytes.
+// Work items: two query tiles each; a shard's leftover odd tile pairs with
+// another shard's over a full lap (the decode below).
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D),
 // O_1 [256+D, 256+2D); P_i overwrites the first 64 columns of S_i as packed
 // bf16 pairs.
