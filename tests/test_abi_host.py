@@ -127,3 +127,37 @@ def test_block_attn_and_merge_and_permute_reject_before_launch():
     assert L.cp_ulysses_head2seq(p, p, 4, 1, 4607, 24, 128, 2, None) == _lib.CP_ERR_INVALID_ARG
     assert L.cp_ulysses_seq2head(p, p, 32, 1, 4608, 24, 128, 2, None) == _lib.CP_ERR_INVALID_ARG
     assert L.cp_debug_bounded_wait_probe(0, None) == _lib.CP_ERR_INVALID_ARG
+
+
+def test_masked_host_buffer_and_anything_entry_points_reject_before_launch():
+    p = 1 << 20
+    L = _lib.lib()
+    # cp_attention_fwd_masked: q, k, v, key_mask, out, lse, B, H, S, D, scale, R, U, ev, ws, ws_bytes, dt, mode, stream
+    m = lambda **kw: L.cp_attention_fwd_masked(p, p, p, kw.get("km", p), p, p, 1, 24, kw.get("S", 4608),
+                                               kw.get("D", 128), 0.088, kw.get("R", 4), kw.get("U", 1),
+                                               kw.get("ev", 0), None, 0, 0, 0, None)
+    assert m(S=4607, R=3, ev=1) == _lib.CP_ERR_UNSUPPORTED_COMBO   # Ring Anything takes no mask
+    assert m(D=96) == _lib.CP_ERR_INVALID_ARG
+    assert m(S=4481) == _lib.CP_ERR_NOT_DIVISIBLE
+    # cp_attention_fwd_host: q, k, v, out, lse (host), B, H, S, D, scale, R, U, ev, dev_buf, dev_bytes, dt, mode,
+    # head_chunks, stream
+    need = cpa.cp_attention_host_buffer_size(1, 24, 4608, 128, 4, 1, torch.bfloat16, "fused")
+    n = 4608 * 24 * 128
+    assert need >= 3 * n * 2 + n * 4 + 24 * 4608 * 4
+    hfn = lambda **kw: L.cp_attention_fwd_host(p, p, p, p, p, kw.get("B", 1), 24, 4608, 128, 0.088, 4, 1, 0,
+                                               kw.get("buf", p), kw.get("nb", need), 0, 0, kw.get("ch", 4), None)
+    assert hfn(ch=0) == _lib.CP_ERR_INVALID_ARG
+    assert hfn(nb=need - 1) == _lib.CP_ERR_WORKSPACE
+    assert hfn(buf=p + 16) == _lib.CP_ERR_ALIGNMENT
+    assert hfn(buf=0) == _lib.CP_ERR_INVALID_ARG
+    assert hfn(B=0) == _lib.CP_OK
+    # Ulysses Anything regroups: U <= H, element size 1, 2, 4 or 8
+    assert L.cp_ulysses_anything_seq2head(p, p, 25, 1, 4481, 24, 128, 2, None) == _lib.CP_ERR_INVALID_ARG
+    assert L.cp_ulysses_anything_head2seq(p, p, 4, 1, 4481, 24, 128, 3, None) == _lib.CP_ERR_INVALID_ARG
+    assert L.cp_ulysses_anything_seq2head(p, p, 5, 0, 4481, 24, 128, 2, None) == _lib.CP_OK
+    # ragged head groups: five regroup launches per head group plus the attention
+    c = cpa.cp_attention_launch_count
+    assert c(1, 24, 4608, 128, 1, 5, torch.bfloat16, "fused") == 1 + 5 * 5
+    assert c(1, 24, 4481, 128, 1, 4, torch.bfloat16, "fused") == 6
+    assert cpa.cp_attention_validate(1, 24, 4481, 128, 1, 4, True) == 0
+    assert cpa.cp_attention_validate(1, 24, 4608, 128, 1, 5, True) == 0
