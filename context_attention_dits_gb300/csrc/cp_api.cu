@@ -418,13 +418,14 @@ size_t cp_attention_workspace_size(int B, int H, int S, int D, int ring_degree, 
 
 int cp_attention_launch_count(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt,
                               cp_lap_mode mode) {
-  (void)H;
-  (void)D;
-  (void)dt;
   if (B == 0 || S == 0) return 0;
   const int R = ring_degree, U = ulysses_degree;
   int n = (mode == CP_LAP_STEPWISE && R > 1) ? R + (R - 1) : 1;
-  if (U > 1 && H % U == 0) n += 3 /* seq2head q, k, v */ + 2 /* head2seq out, lse */;
+  if (U > 1 && H % U == 0) {
+    // q, k, v regroups share one launch when their segments take the bulk path
+    const int64_t seg = static_cast<int64_t>(H / U) * D * (dt == CP_BF16 ? 2 : 4);
+    n += (seg >= 256 && seg <= 24 * 1024 && seg % 16 == 0 ? 1 : 3) + 2 /* head2seq out, lse */;
+  }
   if (U > 1 && H % U != 0) n += 5 * U; /* per head group: q, k, v in; out, lse back */
   return n;
 }
@@ -468,13 +469,16 @@ static cp_status attention_fwd_impl(const void* q, const void* k, const void* v,
   if (U > 1) {
     void* dst[3] = {ws + w.qh, ws + w.kh, ws + w.vh};
     const void* src[3] = {q, k, v};
-    for (int i = 0; i < 3; ++i) {
-      if (!ragged) {
-        // out segments (g, b, t) of Hg*D elements <- in[b, t, g*Hg : (g+1)*Hg, :]
-        SegCopy c{src[i], dst[i], 1, U, B, S, 0, row, static_cast<int64_t>(S) * H * D,
-                  static_cast<int64_t>(H) * D, row, eb};
-        if (cp::launch_segment_copy(c, s) != cudaSuccess) return CP_ERR_CUDA;
-      } else {
+    if (!ragged) {
+      // out segments (g, b, t) of Hg*D elements <- in[b, t, g*Hg : (g+1)*Hg, :], q, k, v in one launch
+      SegCopy cs[3];
+      for (int i = 0; i < 3; ++i)
+        cs[i] = SegCopy{src[i], dst[i], 1, U, B, S, 0, row, static_cast<int64_t>(S) * H * D,
+                        static_cast<int64_t>(H) * D, row, eb};
+      if (cp::launch_segment_copies(cs, 3, s) != cudaSuccess) return CP_ERR_CUDA;
+    }
+    for (int i = 0; i < 3 && ragged; ++i) {
+      {
         for (int g = 0; g < U; ++g) {
           // group g, rows (b, t) of hlen[g]*D elements <- in[b, t, hoff[g] : hoff[g] + hlen[g], :]
           SegCopy c{static_cast<const char*>(src[i]) + static_cast<int64_t>(hoff[g]) * D * eb,

@@ -101,6 +101,8 @@ struct SegCopy {
 // Picks the widest vector (16, 8, 4 or 1 bytes) that every segment start, the
 // segment length and both base pointers allow.
 cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s);
+// n (1..3) copies; copies of one shape that take the bulk path share a launch.
+cudaError_t launch_segment_copies(const SegCopy* cs, int n, cudaStream_t s);
 
 // Device error word of the tensor-core kernel's translation unit.
 uint32_t* device_error_word();  // device address on the current device, or nullptr

@@ -291,8 +291,15 @@ __device__ __forceinline__ bool bulk_bar_wait(uint32_t bar, uint32_t parity, uin
   return true;
 }
 
-__global__ void __launch_bounds__(32) segment_copy_bulk_kernel(const SegCopy c, int64_t per_cta, int K,
-                                                               uint32_t* err, uint64_t timeout_ns) {
+// Up to three same-shaped copies in one launch: blockIdx.y picks the copy.
+struct SegCopyBatch {
+  SegCopy c[3];
+};
+
+__global__ void __launch_bounds__(32) segment_copy_bulk_kernel(const __grid_constant__ SegCopyBatch batch,
+                                                               int64_t per_cta, int K, uint32_t* err,
+                                                               uint64_t timeout_ns) {
+  const SegCopy& c = batch.c[blockIdx.y];
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t bars[kBulkSlots];
   if (threadIdx.x != 0) return;
@@ -402,13 +409,11 @@ cudaError_t launch_lse_merge(float* out_acc, float* lse_acc, const float* out_bl
   return cudaGetLastError();
 }
 
-cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s) {
-  const int64_t nseg = c.n0 * c.n1 * c.n2 * c.n3;
-  if (nseg == 0 || c.seg_elems == 0) return cudaSuccess;
+// Whether copy c can take the bulk path: 16-byte aligned addresses, strides
+// and segments of 256 B to one ring slot, and an output layout that is
+// contiguous in segment order.
+static bool bulk_eligible(const SegCopy& c) {
   const int64_t seg_bytes = c.seg_elems * c.elem_bytes;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   uint64_t align = static_cast<uint64_t>(seg_bytes) | reinterpret_cast<uintptr_t>(c.in) |
                    reinterpret_cast<uintptr_t>(c.out);
   for (int64_t st : {c.st0, c.st1, c.st2, c.st3, c.ost0, c.ost1, c.ost2, c.ost3})
@@ -419,25 +424,53 @@ cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s) {
   const bool natural = (c.n3 == 1 || c.ost3 == nat3) && (c.n2 == 1 || c.ost2 == nat2) &&
                        (c.n1 == 1 || c.ost1 == nat1) && (c.n0 == 1 || c.ost0 == nat0);
   const bool out_contig = (c.ost0 | c.ost1 | c.ost2 | c.ost3) == 0 || natural;
-  if (out_contig && align % 16 == 0 && seg_bytes >= 256 && seg_bytes <= kBulkSlotBytes) {
-    uint32_t* err = device_error_word();
-    if (err == nullptr) return cudaErrorUnknown;
-    static_assert(kBulkSmem <= 227 * 1024, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(segment_copy_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kBulkSmem);
-    if (e != cudaSuccess) return e;
-    const int K = static_cast<int>(kBulkSlotBytes / seg_bytes);
-    // two CTAs per SM (two rings fit in shared memory), at least one chunk each
-    const int64_t chunks = (nseg + K - 1) / K;
-    const int64_t ctas = chunks < 2LL * sms ? chunks : 2LL * sms;
-    const int64_t per_cta = (chunks + ctas - 1) / ctas * K;
-    const int64_t grid = (nseg + per_cta - 1) / per_cta;
-    SegCopy cc = c;
-    cc.ost0 = cc.ost1 = cc.ost2 = cc.ost3 = 0;  // contiguous output
-    segment_copy_bulk_kernel<<<static_cast<unsigned>(grid), 32, kBulkSmem, s>>>(cc, per_cta, K, err,
-                                                                                 kCopyWaitTimeoutNs);
-    return cudaGetLastError();
+  return out_contig && align % 16 == 0 && seg_bytes >= 256 && seg_bytes <= kBulkSlotBytes;
+}
+
+// One bulk launch for n (1..3) eligible copies of the same shape.
+static cudaError_t launch_bulk(const SegCopy* cs, int n, cudaStream_t s) {
+  const SegCopy& c = cs[0];
+  const int64_t nseg = c.n0 * c.n1 * c.n2 * c.n3;
+  const int64_t seg_bytes = c.seg_elems * c.elem_bytes;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  uint32_t* err = device_error_word();
+  if (err == nullptr) return cudaErrorUnknown;
+  static_assert(kBulkSmem <= 227 * 1024, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(segment_copy_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kBulkSmem);
+  if (e != cudaSuccess) return e;
+  const int K = static_cast<int>(kBulkSlotBytes / seg_bytes);
+  // two CTAs per SM (two rings fit in shared memory) shared by the n copies, at least one chunk each
+  const int64_t chunks = (nseg + K - 1) / K;
+  const int64_t cap = (2LL * sms + n - 1) / n;
+  const int64_t ctas = chunks < cap ? chunks : cap;
+  const int64_t per_cta = (chunks + ctas - 1) / ctas * K;
+  const int64_t grid = (nseg + per_cta - 1) / per_cta;
+  SegCopyBatch batch;
+  for (int i = 0; i < n; ++i) {
+    batch.c[i] = cs[i];
+    batch.c[i].ost0 = batch.c[i].ost1 = batch.c[i].ost2 = batch.c[i].ost3 = 0;  // contiguous output
   }
+  for (int i = n; i < 3; ++i) batch.c[i] = batch.c[0];
+  segment_copy_bulk_kernel<<<dim3(static_cast<unsigned>(grid), static_cast<unsigned>(n)), 32, kBulkSmem, s>>>(
+      batch, per_cta, K, err, kCopyWaitTimeoutNs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s) {
+  const int64_t nseg = c.n0 * c.n1 * c.n2 * c.n3;
+  if (nseg == 0 || c.seg_elems == 0) return cudaSuccess;
+  const int64_t seg_bytes = c.seg_elems * c.elem_bytes;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (bulk_eligible(c)) return launch_bulk(&c, 1, s);
+  uint64_t align = static_cast<uint64_t>(seg_bytes) | reinterpret_cast<uintptr_t>(c.in) |
+                   reinterpret_cast<uintptr_t>(c.out);
+  for (int64_t st : {c.st0, c.st1, c.st2, c.st3, c.ost0, c.ost1, c.ost2, c.ost3})
+    align |= static_cast<uint64_t>(st * c.elem_bytes);
   auto launch = [&](auto kernel) {
     int per_sm = 1;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
@@ -454,6 +487,22 @@ cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s) {
   if (align % 8 == 0) return launch(segment_copy_kernel<uint2>);
   if (align % 4 == 0) return launch(segment_copy_kernel<uint32_t>);
   return launch(segment_copy_kernel<uint8_t>);
+}
+
+cudaError_t launch_segment_copies(const SegCopy* cs, int n, cudaStream_t s) {
+  bool same = n >= 1 && n <= 3;
+  for (int i = 0; i < n && same; ++i) {
+    const SegCopy& a = cs[i];
+    same = bulk_eligible(a) && a.n0 == cs[0].n0 && a.n1 == cs[0].n1 && a.n2 == cs[0].n2 && a.n3 == cs[0].n3 &&
+           a.st0 == cs[0].st0 && a.st1 == cs[0].st1 && a.st2 == cs[0].st2 && a.st3 == cs[0].st3 &&
+           a.seg_elems == cs[0].seg_elems && a.elem_bytes == cs[0].elem_bytes;
+  }
+  if (same && cs[0].n0 * cs[0].n1 * cs[0].n2 * cs[0].n3 > 0) return launch_bulk(cs, n, s);
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = launch_segment_copy(cs[i], s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace cp

@@ -86,8 +86,9 @@ def test_workspace_and_launch_counts():
     c = cpa.cp_attention_launch_count
     assert c(1, 24, 4608, 128, 4, 1, torch.bfloat16, "fused") == 1
     assert c(1, 24, 4608, 128, 4, 1, torch.bfloat16, "stepwise") == 7
-    assert c(1, 24, 4608, 128, 1, 4, torch.bfloat16, "fused") == 6
-    assert c(1, 24, 32768, 128, 2, 4, torch.bfloat16, "stepwise") == 8
+    assert c(1, 24, 4608, 128, 1, 4, torch.bfloat16, "fused") == 4  # q, k, v regroups share a launch
+    assert c(1, 24, 4608, 64, 1, 24, torch.bfloat16, "fused") == 6  # 128-byte segments: vector copies
+    assert c(1, 24, 32768, 128, 2, 4, torch.bfloat16, "stepwise") == 6
 
 
 def _raw(fn, *args):
@@ -158,6 +159,6 @@ def test_masked_host_buffer_and_anything_entry_points_reject_before_launch():
     # ragged head groups: five regroup launches per head group plus the attention
     c = cpa.cp_attention_launch_count
     assert c(1, 24, 4608, 128, 1, 5, torch.bfloat16, "fused") == 1 + 5 * 5
-    assert c(1, 24, 4481, 128, 1, 4, torch.bfloat16, "fused") == 6
+    assert c(1, 24, 4481, 128, 1, 4, torch.bfloat16, "fused") == 4
     assert cpa.cp_attention_validate(1, 24, 4481, 128, 1, 4, True) == 0
     assert cpa.cp_attention_validate(1, 24, 4608, 128, 1, 5, True) == 0
