@@ -360,6 +360,7 @@ static cp_status anything_regroup(const void* in, void* out, int U, int B, int S
   const char* src = static_cast<const char*>(in);
   char* dst = static_cast<char*>(out);
   const int64_t HD = static_cast<int64_t>(H) * D;
+  std::vector<SegCopy> cs;
   for (int g = 0; g < U; ++g) {
     const int64_t gD = static_cast<int64_t>(hl[g]) * D;       // elements of a group row
     const int64_t gbase = static_cast<int64_t>(B) * S * ho[g] * D;
@@ -370,14 +371,17 @@ static cp_status anything_regroup(const void* in, void* out, int U, int B, int S
       const int64_t r_el = rbase + static_cast<int64_t>(ho[g]) * D, r_b = sl[u] * HD;
       // group side: rows (b, soff_u + s) of pitch H_g*D, batch stride S*H_g*D
       const int64_t g_el = gbase + static_cast<int64_t>(so[u]) * gD, g_b = S * gD;
-      SegCopy c = to_heads ? SegCopy{src + r_el * eb, dst + g_el * eb, 1, 1, B, sl[u], 0, 0, r_b, HD, gD, eb,
-                                     0, 0, g_b, gD}
-                           : SegCopy{src + g_el * eb, dst + r_el * eb, 1, 1, B, sl[u], 0, 0, g_b, gD, gD, eb,
-                                     0, 0, r_b, HD};
-      if (cp::launch_segment_copy(c, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CP_ERR_CUDA;
+      cs.push_back(to_heads ? SegCopy{src + r_el * eb, dst + g_el * eb, 1, 1, B, sl[u], 0, 0, r_b, HD, gD, eb,
+                                      0, 0, g_b, gD}
+                            : SegCopy{src + g_el * eb, dst + r_el * eb, 1, 1, B, sl[u], 0, 0, g_b, gD, gD, eb,
+                                      0, 0, r_b, HD});
     }
   }
-  return CP_OK;
+  // the U * U copies write disjoint ranges: they share launches
+  return cp::launch_segment_copies(cs.data(), static_cast<int>(cs.size()), static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? CP_OK
+             : CP_ERR_CUDA;
 }
 
 cp_status cp_ulysses_anything_seq2head(const void* in, void* out, int U, int B, int S, int H, int D, int elem_bytes,
@@ -416,17 +420,84 @@ size_t cp_attention_workspace_size(int B, int H, int S, int D, int ring_degree, 
   return ws_layout(B, H, S, D, ring_degree, ulysses_degree, dt, mode).total;
 }
 
+}  // extern "C" (reopened below)
+
+// Copies of the simulated Ulysses all-to-all #1, global [B,S,H,D] -> [U][B,S,Hg,D]
+// with Hg = ceil(H/U), for q, k and v (src -> dst). With H % U != 0 the head
+// groups are a balanced split and a short group leaves its last head slot
+// unwritten (padding).
+static void ulysses_in_copies(const void* const src[3], void* const dst[3], int B, int H, int S, int D, int U, int eb,
+                              std::vector<SegCopy>* cs) {
+  const int Hg = (H + U - 1) / U;
+  const int64_t row = static_cast<int64_t>(Hg) * D;
+  const int64_t grp = static_cast<int64_t>(B) * S * row;  // elements per head group
+  if (H % U == 0) {
+    // out segments (g, b, t) of Hg*D elements <- in[b, t, g*Hg : (g+1)*Hg, :]
+    for (int i = 0; i < 3; ++i)
+      cs->push_back(SegCopy{src[i], dst[i], 1, U, B, S, 0, row, static_cast<int64_t>(S) * H * D,
+                            static_cast<int64_t>(H) * D, row, eb});
+    return;
+  }
+  std::vector<int> hoff(U), hlen(U);
+  (void)shard_table(H, U, true, hoff.data(), hlen.data());
+  for (int i = 0; i < 3; ++i)
+    for (int g = 0; g < U; ++g)
+      // group g, rows (b, t) of hlen[g]*D elements <- in[b, t, hoff[g] : hoff[g] + hlen[g], :]
+      cs->push_back(SegCopy{static_cast<const char*>(src[i]) + static_cast<int64_t>(hoff[g]) * D * eb,
+                            static_cast<char*>(dst[i]) + g * grp * eb, 1, 1, B, S, 0, 0,
+                            static_cast<int64_t>(S) * H * D, static_cast<int64_t>(H) * D,
+                            static_cast<int64_t>(hlen[g]) * D, eb, 0, 0, S * row, row});
+}
+
+// Copies of the simulated Ulysses all-to-all #2: out [U][B,S,Hg,D] -> [B,S,H,D]
+// and lse [U][B,Hg,S] -> [B,H,S], real heads only.
+static void ulysses_out_copies(const float* oa, const float* la, float* out, float* lse, int B, int H, int S, int D,
+                               int U, std::vector<SegCopy>* cs) {
+  const int Hg = (H + U - 1) / U;
+  const int64_t row = static_cast<int64_t>(Hg) * D;
+  const int64_t bstride = S * row;
+  const int64_t grp = static_cast<int64_t>(B) * bstride;
+  if (H % U == 0) {
+    cs->push_back(SegCopy{oa, out, 1, B, S, U, 0, bstride, row, static_cast<int64_t>(B) * bstride, row, 4});
+    cs->push_back(SegCopy{la, lse, 1, B, U, Hg, 0, static_cast<int64_t>(Hg) * S, static_cast<int64_t>(B) * Hg * S,
+                          S, S, 4});
+    return;
+  }
+  std::vector<int> hoff(U), hlen(U);
+  (void)shard_table(H, U, true, hoff.data(), hlen.data());
+  for (int g = 0; g < U; ++g) {
+    // out[b, t, hoff[g] + h, :] <- group g row (b, t)
+    cs->push_back(SegCopy{oa + g * grp, out + static_cast<int64_t>(hoff[g]) * D, 1, 1, B, S, 0, 0, S * row, row,
+                          static_cast<int64_t>(hlen[g]) * D, 4, 0, 0, static_cast<int64_t>(S) * H * D,
+                          static_cast<int64_t>(H) * D});
+    // lse[b, hoff[g] + h, :] <- group g lse[b, h, :]
+    cs->push_back(SegCopy{la + static_cast<int64_t>(g) * B * Hg * S, lse + static_cast<int64_t>(hoff[g]) * S, 1, 1,
+                          B, hlen[g], 0, 0, static_cast<int64_t>(Hg) * S, S, S, 4, 0, 0,
+                          static_cast<int64_t>(H) * S, S});
+  }
+}
+
+extern "C" {
+
 int cp_attention_launch_count(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt,
                               cp_lap_mode mode) {
   if (B == 0 || S == 0) return 0;
   const int R = ring_degree, U = ulysses_degree;
   int n = (mode == CP_LAP_STEPWISE && R > 1) ? R + (R - 1) : 1;
-  if (U > 1 && H % U == 0) {
-    // q, k, v regroups share one launch when their segments take the bulk path
-    const int64_t seg = static_cast<int64_t>(H / U) * D * (dt == CP_BF16 ? 2 : 4);
-    n += (seg >= 256 && seg <= 24 * 1024 && seg % 16 == 0 ? 1 : 3) + 2 /* head2seq out, lse */;
+  if (U > 1 && U <= H && D > 0) {
+    // the same copy descriptors as a call makes, on stand-in addresses with
+    // the alignment (256 B) of the caller's buffers and the workspace
+    const WsLayout w = ws_layout(B, H, S, D, R, U, dt, mode);
+    char* base = reinterpret_cast<char*>(uintptr_t{1} << 20);
+    const void* src[3] = {base, base, base};
+    void* dst[3] = {base + w.qh, base + w.kh, base + w.vh};
+    std::vector<SegCopy> in, out;
+    ulysses_in_copies(src, dst, B, H, S, D, U, elem_size(dt), &in);
+    ulysses_out_copies(reinterpret_cast<float*>(base + w.oh), reinterpret_cast<float*>(base + w.lh),
+                       reinterpret_cast<float*>(base), reinterpret_cast<float*>(base), B, H, S, D, U, &out);
+    n += cp::segment_copy_launches(in.data(), static_cast<int>(in.size())) +
+         cp::segment_copy_launches(out.data(), static_cast<int>(out.size()));
   }
-  if (U > 1 && H % U != 0) n += 5 * U; /* per head group: q, k, v in; out, lse back */
   return n;
 }
 
@@ -457,10 +528,7 @@ static cp_status attention_fwd_impl(const void* q, const void* k, const void* v,
   // a short group being padding that the attention kernels skip
   const int Hg = (H + U - 1) / U, Bn = B * U;
   const bool ragged = H % U != 0;
-  std::vector<int> hoff(U), hlen(U);
-  if (shard_table(H, U, true, hoff.data(), hlen.data()) != CP_OK) return CP_ERR_INVALID_ARG;
   const int64_t row = static_cast<int64_t>(Hg) * D;
-  const int64_t grp = static_cast<int64_t>(B) * S * row;  // elements per head group
 
   // --- Ulysses all-to-all #1 (simulated): global [B,S,H,D] -> [U][B,S,Hg,D] ---
   const void *qa = q, *ka = k, *va = v;
@@ -469,26 +537,9 @@ static cp_status attention_fwd_impl(const void* q, const void* k, const void* v,
   if (U > 1) {
     void* dst[3] = {ws + w.qh, ws + w.kh, ws + w.vh};
     const void* src[3] = {q, k, v};
-    if (!ragged) {
-      // out segments (g, b, t) of Hg*D elements <- in[b, t, g*Hg : (g+1)*Hg, :], q, k, v in one launch
-      SegCopy cs[3];
-      for (int i = 0; i < 3; ++i)
-        cs[i] = SegCopy{src[i], dst[i], 1, U, B, S, 0, row, static_cast<int64_t>(S) * H * D,
-                        static_cast<int64_t>(H) * D, row, eb};
-      if (cp::launch_segment_copies(cs, 3, s) != cudaSuccess) return CP_ERR_CUDA;
-    }
-    for (int i = 0; i < 3 && ragged; ++i) {
-      {
-        for (int g = 0; g < U; ++g) {
-          // group g, rows (b, t) of hlen[g]*D elements <- in[b, t, hoff[g] : hoff[g] + hlen[g], :]
-          SegCopy c{static_cast<const char*>(src[i]) + static_cast<int64_t>(hoff[g]) * D * eb,
-                    static_cast<char*>(dst[i]) + g * grp * eb, 1, 1, B, S, 0, 0,
-                    static_cast<int64_t>(S) * H * D, static_cast<int64_t>(H) * D,
-                    static_cast<int64_t>(hlen[g]) * D, eb, 0, 0, S * row, row};
-          if (cp::launch_segment_copy(c, s) != cudaSuccess) return CP_ERR_CUDA;
-        }
-      }
-    }
+    std::vector<SegCopy> cs;  // disjoint outputs: they share launches
+    ulysses_in_copies(src, dst, B, H, S, D, U, eb, &cs);
+    if (cp::launch_segment_copies(cs.data(), static_cast<int>(cs.size()), s) != cudaSuccess) return CP_ERR_CUDA;
     qa = dst[0];
     ka = dst[1];
     va = dst[2];
@@ -527,24 +578,11 @@ static cp_status attention_fwd_impl(const void* q, const void* k, const void* v,
     }
   }
 
-  // --- Ulysses all-to-all #2 (simulated): [U][B,S,H/U,D] -> [B,S,H,D]; lse [U][B,H/U,S] -> [B,H,S] ---
-  if (U > 1 && !ragged) {
-    SegCopy co{oa, out, 1, B, S, U, 0, bstride, row, static_cast<int64_t>(B) * bstride, row, 4};
-    if (cp::launch_segment_copy(co, s) != cudaSuccess) return CP_ERR_CUDA;
-    SegCopy cl{la, lse, 1, B, U, Hg, 0, static_cast<int64_t>(Hg) * S, static_cast<int64_t>(B) * Hg * S, S, S, 4};
-    if (cp::launch_segment_copy(cl, s) != cudaSuccess) return CP_ERR_CUDA;
-  } else if (U > 1) {
-    for (int g = 0; g < U; ++g) {
-      // out[b, t, hoff[g] + h, :] <- group g row (b, t), real heads only
-      SegCopy co{oa + g * grp, out + static_cast<int64_t>(hoff[g]) * D, 1, 1, B, S, 0, 0, S * row, row,
-                 static_cast<int64_t>(hlen[g]) * D, 4, 0, 0, static_cast<int64_t>(S) * H * D,
-                 static_cast<int64_t>(H) * D};
-      if (cp::launch_segment_copy(co, s) != cudaSuccess) return CP_ERR_CUDA;
-      // lse[b, hoff[g] + h, :] <- group g lse[b, h, :]
-      SegCopy cl{la + static_cast<int64_t>(g) * B * Hg * S, lse + static_cast<int64_t>(hoff[g]) * S, 1, 1, B,
-                 hlen[g], 0, 0, static_cast<int64_t>(Hg) * S, S, S, 4, 0, 0, static_cast<int64_t>(H) * S, S};
-      if (cp::launch_segment_copy(cl, s) != cudaSuccess) return CP_ERR_CUDA;
-    }
+  // --- Ulysses all-to-all #2 (simulated): [U][B,S,Hg,D] -> [B,S,H,D]; lse [U][B,Hg,S] -> [B,H,S] ---
+  if (U > 1) {
+    std::vector<SegCopy> cs;
+    ulysses_out_copies(oa, la, out, lse, B, H, S, D, U, &cs);
+    if (cp::launch_segment_copies(cs.data(), static_cast<int>(cs.size()), s) != cudaSuccess) return CP_ERR_CUDA;
   }
   return CP_OK;
 }

@@ -101,8 +101,13 @@ struct SegCopy {
 // Picks the widest vector (16, 8, 4 or 1 bytes) that every segment start, the
 // segment length and both base pointers allow.
 cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s);
-// n (1..3) copies; copies of one shape that take the bulk path share a launch.
+// n copies in stream order of launches: the copies that take the bulk path
+// (16-byte aligned, segments of 256 B to 24 KB) share launches, up to 24 per
+// launch; every other copy takes a launch of its own.
 cudaError_t launch_segment_copies(const SegCopy* cs, int n, cudaStream_t s);
+// The number of launches launch_segment_copies makes for the same copies
+// (pointers need only carry their alignment).
+int segment_copy_launches(const SegCopy* cs, int n);
 
 // Device error word of the tensor-core kernel's translation unit.
 uint32_t* device_error_word();  // device address on the current device, or nullptr

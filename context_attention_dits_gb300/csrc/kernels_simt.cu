@@ -291,49 +291,70 @@ __device__ __forceinline__ bool bulk_bar_wait(uint32_t bar, uint32_t parity, uin
   return true;
 }
 
-// Up to three same-shaped copies in one launch: blockIdx.y picks the copy.
-struct SegCopyBatch {
-  SegCopy c[3];
+// One copy of a batch: its descriptor (all output strides 0 when the output
+// is contiguous in segment order), segments per CTA and segments per ring slot.
+struct BulkCopy {
+  SegCopy c;
+  int64_t per_cta;
+  int K;
+};
+constexpr int kMaxBulkBatch = 24;
+struct BulkBatch {
+  BulkCopy d[kMaxBulkBatch];
 };
 
-__global__ void __launch_bounds__(32) segment_copy_bulk_kernel(const __grid_constant__ SegCopyBatch batch,
-                                                               int64_t per_cta, int K, uint32_t* err,
-                                                               uint64_t timeout_ns) {
-  const SegCopy& c = batch.c[blockIdx.y];
+// Position of one segment in (i0, i1, i2, i3) order and its element offset
+// under strides (s0, s1, s2, s3).
+struct SegIter {
+  int64_t i1, i2, i3, el;
+  __device__ __forceinline__ void init(const SegCopy& c, int64_t sg, int64_t s0, int64_t s1, int64_t s2, int64_t s3) {
+    i3 = sg % c.n3;
+    sg /= c.n3;
+    i2 = sg % c.n2;
+    sg /= c.n2;
+    i1 = sg % c.n1;
+    el = (sg / c.n1) * s0 + i1 * s1 + i2 * s2 + i3 * s3;
+  }
+  __device__ __forceinline__ void next(const SegCopy& c, int64_t s0, int64_t s1, int64_t s2, int64_t s3) {
+    el += s3;
+    if (++i3 == c.n3) {
+      i3 = 0;
+      el += s2 - c.n3 * s3;
+      if (++i2 == c.n2) {
+        i2 = 0;
+        el += s1 - c.n2 * s2;
+        if (++i1 == c.n1) {
+          i1 = 0;
+          el += s0 - c.n1 * s1;
+        }
+      }
+    }
+  }
+};
+
+// blockIdx.y picks the copy of the batch, blockIdx.x its range of segments.
+__global__ void __launch_bounds__(32) segment_copy_bulk_kernel(const __grid_constant__ BulkBatch batch,
+                                                               uint32_t* err, uint64_t timeout_ns) {
+  const BulkCopy& d = batch.d[blockIdx.y];
+  const SegCopy& c = d.c;
+  const int64_t per_cta = d.per_cta;
+  const int K = d.K;
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t bars[kBulkSlots];
   if (threadIdx.x != 0) return;
   const int64_t nseg = c.n0 * c.n1 * c.n2 * c.n3;
   const int64_t seg_bytes = c.seg_elems * c.elem_bytes;
-  int64_t sg0 = static_cast<int64_t>(blockIdx.x) * per_cta;
+  const int64_t sg0 = static_cast<int64_t>(blockIdx.x) * per_cta;
   const int64_t end = sg0 + per_cta < nseg ? sg0 + per_cta : nseg;
   if (sg0 >= end) return;
   for (int i = 0; i < kBulkSlots; ++i) mbar_init(smem_addr(&bars[i]), 1);
   fence_mbar_init();
   const char* in = static_cast<const char*>(c.in);
   char* out = static_cast<char*>(c.out);
-  int64_t rest = sg0;
-  int64_t i3 = rest % c.n3;
-  rest /= c.n3;
-  int64_t i2 = rest % c.n2;
-  rest /= c.n2;
-  int64_t i1 = rest % c.n1;
-  int64_t src_el = (rest / c.n1) * c.st0 + i1 * c.st1 + i2 * c.st2 + i3 * c.st3;
-  auto advance = [&]() {  // to the next segment in (i0, i1, i2, i3) order
-    src_el += c.st3;
-    if (++i3 == c.n3) {
-      i3 = 0;
-      src_el += c.st2 - c.n3 * c.st3;
-      if (++i2 == c.n2) {
-        i2 = 0;
-        src_el += c.st1 - c.n2 * c.st2;
-        if (++i1 == c.n1) {
-          i1 = 0;
-          src_el += c.st0 - c.n1 * c.st1;
-        }
-      }
-    }
-  };
+  const bool strided_out = (c.ost0 | c.ost1 | c.ost2 | c.ost3) != 0;
+  SegIter src, dst;  // next segment to load, next segment to store (strided output)
+  src.init(c, sg0, c.st0, c.st1, c.st2, c.st3);
+  dst.init(c, sg0, c.ost0, c.ost1, c.ost2, c.ost3);
   const int64_t nchunks = (end - sg0 + K - 1) / K;
   const uint32_t ring0 = smem_addr(ring);
   int64_t loaded = 0;  // chunks whose loads were issued
@@ -347,9 +368,9 @@ __global__ void __launch_bounds__(32) segment_copy_bulk_kernel(const __grid_cons
       const uint32_t bar = smem_addr(&bars[slot]);
       mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * seg_bytes));
       for (int k = 0; k < n; ++k) {
-        bulk_load(ring0 + slot * kBulkSlotBytes + static_cast<uint32_t>(k * seg_bytes), in + src_el * c.elem_bytes,
+        bulk_load(ring0 + slot * kBulkSlotBytes + static_cast<uint32_t>(k * seg_bytes), in + src.el * c.elem_bytes,
                   static_cast<uint32_t>(seg_bytes), bar);
-        advance();
+        src.next(c, c.st0, c.st1, c.st2, c.st3);
       }
       ++loaded;
     }
@@ -363,7 +384,15 @@ __global__ void __launch_bounds__(32) segment_copy_bulk_kernel(const __grid_cons
       }
       const int64_t first = sg0 + cj * K;
       const int64_t n = end - first < K ? end - first : K;
-      bulk_store(out + first * seg_bytes, ring0 + slot * kBulkSlotBytes, static_cast<uint32_t>(n * seg_bytes));
+      if (!strided_out) {
+        bulk_store(out + first * seg_bytes, ring0 + slot * kBulkSlotBytes, static_cast<uint32_t>(n * seg_bytes));
+      } else {
+        for (int64_t k = 0; k < n; ++k) {
+          bulk_store(out + dst.el * c.elem_bytes, ring0 + slot * kBulkSlotBytes + static_cast<uint32_t>(k * seg_bytes),
+                     static_cast<uint32_t>(seg_bytes));
+          dst.next(c, c.ost0, c.ost1, c.ost2, c.ost3);
+        }
+      }
     }
   }
   if (!ok) {
@@ -409,64 +438,81 @@ cudaError_t launch_lse_merge(float* out_acc, float* lse_acc, const float* out_bl
   return cudaGetLastError();
 }
 
-// Whether copy c can take the bulk path: 16-byte aligned addresses, strides
-// and segments of 256 B to one ring slot, and an output layout that is
-// contiguous in segment order.
+static int sm_count() {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+// Whether copy c can take the bulk path: 16-byte aligned addresses and
+// strides, and segments of 256 B to one ring slot.
 static bool bulk_eligible(const SegCopy& c) {
   const int64_t seg_bytes = c.seg_elems * c.elem_bytes;
   uint64_t align = static_cast<uint64_t>(seg_bytes) | reinterpret_cast<uintptr_t>(c.in) |
                    reinterpret_cast<uintptr_t>(c.out);
   for (int64_t st : {c.st0, c.st1, c.st2, c.st3, c.ost0, c.ost1, c.ost2, c.ost3})
     align |= static_cast<uint64_t>(st * c.elem_bytes);
-  // output strides that describe the contiguous layout allow the bulk path
-  // (a stride of a dimension of extent 1 never matters)
-  const int64_t nat3 = c.seg_elems, nat2 = c.n3 * nat3, nat1 = c.n2 * nat2, nat0 = c.n1 * nat1;
-  const bool natural = (c.n3 == 1 || c.ost3 == nat3) && (c.n2 == 1 || c.ost2 == nat2) &&
-                       (c.n1 == 1 || c.ost1 == nat1) && (c.n0 == 1 || c.ost0 == nat0);
-  const bool out_contig = (c.ost0 | c.ost1 | c.ost2 | c.ost3) == 0 || natural;
-  return out_contig && align % 16 == 0 && seg_bytes >= 256 && seg_bytes <= kBulkSlotBytes;
+  return align % 16 == 0 && seg_bytes >= 256 && seg_bytes <= kBulkSlotBytes;
 }
 
-// One bulk launch for n (1..3) eligible copies of the same shape.
-static cudaError_t launch_bulk(const SegCopy* cs, int n, cudaStream_t s) {
-  const SegCopy& c = cs[0];
-  const int64_t nseg = c.n0 * c.n1 * c.n2 * c.n3;
-  const int64_t seg_bytes = c.seg_elems * c.elem_bytes;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+// c with all output strides 0 when they describe the contiguous layout (a
+// stride of a dimension of extent 1 never matters), so that the kernel
+// stores whole chunks.
+static SegCopy normalise_out(SegCopy c) {
+  const int64_t nat3 = c.seg_elems, nat2 = c.n3 * nat3, nat1 = c.n2 * nat2, nat0 = c.n1 * nat1;
+  if ((c.n3 == 1 || c.ost3 == nat3) && (c.n2 == 1 || c.ost2 == nat2) && (c.n1 == 1 || c.ost1 == nat1) &&
+      (c.n0 == 1 || c.ost0 == nat0))
+    c.ost0 = c.ost1 = c.ost2 = c.ost3 = 0;
+  return c;
+}
+
+static int64_t seg_count(const SegCopy& c) { return c.n0 * c.n1 * c.n2 * c.n3; }
+
+// One bulk launch for n (1..kMaxBulkBatch) eligible, non-empty copies. Two
+// CTAs per SM (two rings fit in shared memory), split among the copies in
+// proportion to their chunks, at least one each.
+static cudaError_t launch_bulk(const SegCopy* const* cs, int n, cudaStream_t s) {
   uint32_t* err = device_error_word();
   if (err == nullptr) return cudaErrorUnknown;
   static_assert(kBulkSmem <= 227 * 1024, "shared memory budget");
+  static_assert(sizeof(BulkBatch) <= 4096, "kernel parameter space");
   cudaError_t e = cudaFuncSetAttribute(segment_copy_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kBulkSmem);
   if (e != cudaSuccess) return e;
-  const int K = static_cast<int>(kBulkSlotBytes / seg_bytes);
-  // two CTAs per SM (two rings fit in shared memory) shared by the n copies, at least one chunk each
-  const int64_t chunks = (nseg + K - 1) / K;
-  const int64_t cap = (2LL * sms + n - 1) / n;
-  const int64_t ctas = chunks < cap ? chunks : cap;
-  const int64_t per_cta = (chunks + ctas - 1) / ctas * K;
-  const int64_t grid = (nseg + per_cta - 1) / per_cta;
-  SegCopyBatch batch;
+  const int64_t budget = 2LL * sm_count();
+  int64_t chunks[kMaxBulkBatch], total = 0;
   for (int i = 0; i < n; ++i) {
-    batch.c[i] = cs[i];
-    batch.c[i].ost0 = batch.c[i].ost1 = batch.c[i].ost2 = batch.c[i].ost3 = 0;  // contiguous output
+    const int64_t K = kBulkSlotBytes / (cs[i]->seg_elems * cs[i]->elem_bytes);
+    chunks[i] = (seg_count(*cs[i]) + K - 1) / K;
+    total += chunks[i];
   }
-  for (int i = n; i < 3; ++i) batch.c[i] = batch.c[0];
+  BulkBatch batch;
+  int64_t grid = 1;
+  for (int i = 0; i < kMaxBulkBatch; ++i) {
+    BulkCopy& d = batch.d[i];
+    d.c = normalise_out(*cs[i < n ? i : 0]);
+    d.K = static_cast<int>(kBulkSlotBytes / (d.c.seg_elems * d.c.elem_bytes));
+    if (i >= n) {  // unused entries: never read (gridDim.y == n)
+      d.per_cta = 1;
+      continue;
+    }
+    int64_t ctas = budget * chunks[i] / total;
+    ctas = ctas < 1 ? 1 : (ctas > chunks[i] ? chunks[i] : ctas);
+    d.per_cta = (chunks[i] + ctas - 1) / ctas * d.K;
+    const int64_t g = (seg_count(d.c) + d.per_cta - 1) / d.per_cta;
+    grid = g > grid ? g : grid;
+  }
   segment_copy_bulk_kernel<<<dim3(static_cast<unsigned>(grid), static_cast<unsigned>(n)), 32, kBulkSmem, s>>>(
-      batch, per_cta, K, err, kCopyWaitTimeoutNs);
+      batch, err, kCopyWaitTimeoutNs);
   return cudaGetLastError();
 }
 
-cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s) {
-  const int64_t nseg = c.n0 * c.n1 * c.n2 * c.n3;
-  if (nseg == 0 || c.seg_elems == 0) return cudaSuccess;
+// One launch of the vector kernel for copy c.
+static cudaError_t launch_vector(const SegCopy& c, cudaStream_t s) {
+  const int64_t nseg = seg_count(c);
   const int64_t seg_bytes = c.seg_elems * c.elem_bytes;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (bulk_eligible(c)) return launch_bulk(&c, 1, s);
+  const int sms = sm_count();
   uint64_t align = static_cast<uint64_t>(seg_bytes) | reinterpret_cast<uintptr_t>(c.in) |
                    reinterpret_cast<uintptr_t>(c.out);
   for (int64_t st : {c.st0, c.st1, c.st2, c.st3, c.ost0, c.ost1, c.ost2, c.ost3})
@@ -489,20 +535,39 @@ cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s) {
   return launch(segment_copy_kernel<uint8_t>);
 }
 
-cudaError_t launch_segment_copies(const SegCopy* cs, int n, cudaStream_t s) {
-  bool same = n >= 1 && n <= 3;
-  for (int i = 0; i < n && same; ++i) {
-    const SegCopy& a = cs[i];
-    same = bulk_eligible(a) && a.n0 == cs[0].n0 && a.n1 == cs[0].n1 && a.n2 == cs[0].n2 && a.n3 == cs[0].n3 &&
-           a.st0 == cs[0].st0 && a.st1 == cs[0].st1 && a.st2 == cs[0].st2 && a.st3 == cs[0].st3 &&
-           a.seg_elems == cs[0].seg_elems && a.elem_bytes == cs[0].elem_bytes;
-  }
-  if (same && cs[0].n0 * cs[0].n1 * cs[0].n2 * cs[0].n3 > 0) return launch_bulk(cs, n, s);
+// The bulk-eligible, non-empty copies go in batches of up to kMaxBulkBatch;
+// every other non-empty copy takes a vector launch of its own. Returns the
+// number of launches, or -1 on a launch error (when s is used).
+static int segment_copies(const SegCopy* cs, int n, cudaStream_t s, bool launch) {
+  const SegCopy* batch[kMaxBulkBatch];
+  int nb = 0, launches = 0;
   for (int i = 0; i < n; ++i) {
-    cudaError_t e = launch_segment_copy(cs[i], s);
-    if (e != cudaSuccess) return e;
+    if (seg_count(cs[i]) == 0 || cs[i].seg_elems == 0) continue;
+    if (!bulk_eligible(cs[i])) {
+      ++launches;
+      if (launch && launch_vector(cs[i], s) != cudaSuccess) return -1;
+      continue;
+    }
+    batch[nb++] = &cs[i];
+    if (nb == kMaxBulkBatch) {
+      ++launches;
+      if (launch && launch_bulk(batch, nb, s) != cudaSuccess) return -1;
+      nb = 0;
+    }
   }
-  return cudaSuccess;
+  if (nb > 0) {
+    ++launches;
+    if (launch && launch_bulk(batch, nb, s) != cudaSuccess) return -1;
+  }
+  return launches;
 }
+
+cudaError_t launch_segment_copies(const SegCopy* cs, int n, cudaStream_t s) {
+  return segment_copies(cs, n, s, true) < 0 ? cudaErrorLaunchFailure : cudaSuccess;
+}
+
+cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s) { return launch_segment_copies(&c, 1, s); }
+
+int segment_copy_launches(const SegCopy* cs, int n) { return segment_copies(cs, n, nullptr, false); }
 
 }  // namespace cp

@@ -86,9 +86,12 @@ def test_workspace_and_launch_counts():
     c = cpa.cp_attention_launch_count
     assert c(1, 24, 4608, 128, 4, 1, torch.bfloat16, "fused") == 1
     assert c(1, 24, 4608, 128, 4, 1, torch.bfloat16, "stepwise") == 7
-    assert c(1, 24, 4608, 128, 1, 4, torch.bfloat16, "fused") == 4  # q, k, v regroups share a launch
-    assert c(1, 24, 4608, 64, 1, 24, torch.bfloat16, "fused") == 6  # 128-byte segments: vector copies
-    assert c(1, 24, 32768, 128, 2, 4, torch.bfloat16, "stepwise") == 6
+    # Ulysses: q, k, v regroups share one bulk launch, out and lse another
+    assert c(1, 24, 4608, 128, 1, 4, torch.bfloat16, "fused") == 3
+    # 128-byte q, k, v segments take a vector launch each
+    assert c(1, 24, 4608, 64, 1, 24, torch.bfloat16, "fused") == 5
+    # 128 KB lse rows exceed a ring slot: out and lse launch separately
+    assert c(1, 24, 32768, 128, 2, 4, torch.bfloat16, "stepwise") == 3 + 1 + 2
 
 
 def _raw(fn, *args):
@@ -156,9 +159,10 @@ def test_masked_host_buffer_and_anything_entry_points_reject_before_launch():
     assert L.cp_ulysses_anything_seq2head(p, p, 25, 1, 4481, 24, 128, 2, None) == _lib.CP_ERR_INVALID_ARG
     assert L.cp_ulysses_anything_head2seq(p, p, 4, 1, 4481, 24, 128, 3, None) == _lib.CP_ERR_INVALID_ARG
     assert L.cp_ulysses_anything_seq2head(p, p, 5, 0, 4481, 24, 128, 2, None) == _lib.CP_OK
-    # ragged head groups: five regroup launches per head group plus the attention
+    # ragged head groups: the 15 per-group q, k, v copies share a launch, the 10 out / lse copies another
     c = cpa.cp_attention_launch_count
-    assert c(1, 24, 4608, 128, 1, 5, torch.bfloat16, "fused") == 1 + 5 * 5
+    assert c(1, 24, 4608, 128, 1, 5, torch.bfloat16, "fused") == 3
+    # 4481-float lse rows are not 16-byte multiples: the lse regroup takes a vector launch
     assert c(1, 24, 4481, 128, 1, 4, torch.bfloat16, "fused") == 4
     assert cpa.cp_attention_validate(1, 24, 4481, 128, 1, 4, True) == 0
     assert cpa.cp_attention_validate(1, 24, 4608, 128, 1, 5, True) == 0

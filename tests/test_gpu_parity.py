@@ -109,6 +109,8 @@ def test_permutes_bit_exact(U, B, S, H, D, dtype):
     (4, 1, 9, 5, 128, torch.bfloat16),
     (2, 3, 7, 3, 8, torch.float32),
     (3, 1, 2, 4, 16, torch.bfloat16),       # fewer tokens than ranks: an empty shard
+    (6, 2, 1000, 12, 128, torch.bfloat16),  # 36 bulk copies with strided batch rows: two launches of <= 24
+    (5, 2, 4481, 24, 128, torch.bfloat16),  # ragged heads and tokens, two batch entries
 ])
 def test_anything_permutes_bit_exact(U, B, S, H, D, dtype):
     from oracle import cp_oracle as co
