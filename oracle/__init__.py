@@ -13,6 +13,8 @@ from .cp_oracle import (
     NotDivisibleError,
     UnsupportedComboError,
     attention,
+    attention_bwd,
+    attention_delta,
     attention_rows,
     head2seq,
     lse_merge,
@@ -22,12 +24,18 @@ from .cp_oracle import (
     ulysses_attention,
     unified_attention,
     cp_attention,
+    cp_attention_bwd,
+    ring_attention_bwd,
 )
 
 __all__ = [
     "NotDivisibleError",
     "UnsupportedComboError",
     "attention",
+    "attention_bwd",
+    "attention_delta",
+    "cp_attention_bwd",
+    "ring_attention_bwd",
     "attention_rows",
     "head2seq",
     "lse_merge",

@@ -411,3 +411,132 @@ def cp_attention(q, k, v, scale: float, ring_degree: int = 1, ulysses_degree: in
     if R == 1:
         return ulysses_attention(q, k, v, scale, U, key_mask)
     return unified_attention(q, k, v, scale, R, U, key_mask)
+
+
+# ---------------------------------------------------------------------------
+# Backward (training). The [CP] variants table and its Ring Anything note mark
+# Ring Anything as inference only; the other variants carry no such note, so
+# they serve training too. The pages write no backward formulas. Reading R18:
+# the gradients are the exact derivatives of L = sum(out * dout) with respect
+# to q, k and v for the forward above, in the form that reuses the forward's
+# lse. Per batch b and head h, with s_ij = scale * q_i . k_j:
+#     p_ij    = exp(s_ij - lse_i)            (the softmax weights)
+#     delta_i = sum_d dout_id * out_id      (= sum_j p_ij dp_ij)
+#     dv_j    = sum_i p_ij dout_i
+#     dp_ij   = dout_i . v_j
+#     ds_ij   = p_ij (dp_ij - delta_i)
+#     dq_i    = scale * sum_j ds_ij k_j
+#     dk_j    = scale * sum_i ds_ij q_i
+# In a ring lap the sums over j split over the K/V blocks and the sums over i
+# over the query shards: at step t rank r adds block (r - t) mod N's share to
+# its dq, and block j's dk and dv collect the shares of the ranks the block
+# visits (j, j+1, ... mod N) and travel with it. In float64 the order of these
+# additions does not matter.
+# ---------------------------------------------------------------------------
+def attention_delta(out, dout):
+    """delta [B, H, S] = sum over d of out[b, s, h, d] * dout[b, s, h, d]."""
+    out, dout = _f64(out), _f64(dout)
+    return np.transpose(np.sum(out * dout, axis=3), (0, 2, 1))
+
+
+def attention_bwd(q, k, v, dout, scale: float, lse, delta):
+    """Gradient shares of one query shard against one K/V block.
+
+    q, dout: [B, Sq, H, D]; k, v: [B, Skv, H, D]; lse, delta: [B, H, Sq], the
+    global values of the shard's rows (after the whole lap). Returns
+    (dq [B, Sq, H, D], dk [B, Skv, H, D], dv [B, Skv, H, D]). A row with
+    lse = -inf (it saw no key) has p = 0 and contributes nothing.
+    """
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    lse, delta = _f64(lse), _f64(delta)
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    dq = np.zeros((B, Sq, H, D))
+    dk = np.zeros((B, Skv, H, D))
+    dv = np.zeros((B, Skv, H, D))
+    if Sq == 0 or Skv == 0:
+        return dq, dk, dv
+    for b in range(B):
+        for h in range(H):
+            qb, kb, vb, gb = q[b, :, h, :], k[b, :, h, :], v[b, :, h, :], dout[b, :, h, :]
+            s = scale * (qb @ kb.T)
+            live = np.isfinite(lse[b, h])
+            p = np.where(live[:, None], np.exp(s - np.where(live, lse[b, h], 0.0)[:, None]), 0.0)
+            dv[b, :, h, :] = p.T @ gb
+            dp = gb @ vb.T
+            ds = p * (dp - delta[b, h][:, None])
+            dq[b, :, h, :] = scale * (ds @ kb)
+            dk[b, :, h, :] = scale * (ds.T @ qb)
+    return dq, dk, dv
+
+
+def ring_attention_bwd(q, k, v, dout, scale: float, ring_degree: int, out=None, lse=None):
+    """Simulated backward ring lap over ``ring_degree`` even shards.
+
+    out, lse: the forward's global results (computed here when omitted).
+    Returns (dq, dk, dv), each [B, S, H, D].
+    """
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    if out is None:
+        out, lse = ring_attention(q, k, v, scale, ring_degree)
+    delta = attention_delta(out, dout)
+    lse = _f64(lse)
+    B, S, H, D = q.shape
+    table = ring_shard_table(S, ring_degree, False)
+    n = len(table)
+    dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    for r, (qo, ql) in enumerate(table):
+        rows = slice(qo, qo + ql)
+        for t in range(n):
+            ko, kl = table[(r - t) % n]
+            keys = slice(ko, ko + kl)
+            gq, gk, gv = attention_bwd(q[:, rows], k[:, keys], v[:, keys], dout[:, rows], scale,
+                                       lse[:, :, rows], delta[:, :, rows])
+            dq[:, rows] += gq
+            dk[:, keys] += gk
+            dv[:, keys] += gv
+    return dq, dk, dv
+
+
+def cp_attention_bwd(q, k, v, dout, scale: float, ring_degree: int = 1, ulysses_degree: int = 1,
+                     uneven_ok: bool = False, out=None, lse=None):
+    """Backward of ``cp_attention`` for the training variants (R18).
+
+    Ring: the backward lap above. Ulysses / Unified: the forward's all-to-all
+    regroups of q, k, v, dout, out and lse (lse head slices), the ring
+    backward inside each head group (ring degree 1 for plain Ulysses), and the
+    inverse regroup of dq, dk and dv. The Anything variants raise
+    UnsupportedComboError: Ring Anything is inference only ([CP] variants
+    table), and Ulysses Anything is left to the forward (reading R19).
+    """
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, S, H, D = q.shape
+    R, U = ring_degree, ulysses_degree
+    if R < 1 or U < 1:
+        raise ValueError("degrees must be >= 1")
+    if uneven_ok:
+        raise UnsupportedComboError("the Anything variants have no backward")
+    if U > H:
+        raise ValueError(f"ulysses_degree {U} exceeds the number of heads {H}")
+    if S % R:
+        raise NotDivisibleError(f"sequence length {S} is not divisible by ring_degree {R}")
+    if out is None:
+        out, lse = cp_attention(q, k, v, scale, R, U)
+    out, lse = _f64(out), _f64(lse)
+    if U == 1:
+        return ring_attention_bwd(q, k, v, dout, scale, R, out, lse)
+    if S % (R * U) or H % U:
+        raise NotDivisibleError(f"S={S} must be divisible by {R * U} and H={H} by {U}")
+    # head group g holds every token of heads [g*H/U, (g+1)*H/U); within a ring
+    # row the seq2head regroup keeps token order, so group g's tokens are in
+    # global order and its ring shards are the contiguous S/R ranges
+    Hg = H // U
+    grads = [np.zeros((U, B, S, Hg, D)) for _ in range(3)]
+    groups = [seq2head(_split_seq(t, U)) for t in (q, k, v, dout, out)]
+    for g in range(U):
+        lse_g = lse[:, g * Hg:(g + 1) * Hg, :]
+        res = ring_attention_bwd(groups[0][g], groups[1][g], groups[2][g], groups[3][g], scale, R,
+                                 groups[4][g], lse_g)
+        for i in range(3):
+            grads[i][g] = res[i]
+    return tuple(np.concatenate(list(head2seq(gr)), axis=1) for gr in grads)

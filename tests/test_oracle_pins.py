@@ -572,3 +572,164 @@ def test_planted_mask_on_queries_is_caught():
     # the mistake: drop the masked positions from the queries instead of the keys
     wrong = oracle.attention(q, k, v, 0.6)[0] * km[:, :, None, None]
     assert np.max(np.abs(wrong - o)) > 1e-3
+
+
+# ----------------------------------------------------------------------------
+# backward (reading R18): pinned to finite differences of the pinned forward,
+# to torch autograd of a plain softmax attention, to invariants of the
+# softmax Jacobian and to closed forms; then planted mistakes
+# ----------------------------------------------------------------------------
+def _loss(q, k, v, dout, scale):
+    return float(np.sum(brute_attention(q, k, v, scale)[0] * dout))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_bwd_matches_central_differences(seed):
+    B, S, Skv, H, D, scale = 1, 3, 4, 2, 3, 0.6
+    q, k, v = rnd((B, S, H, D), 200 + seed), rnd((B, Skv, H, D), 210 + seed), rnd((B, Skv, H, D), 220 + seed)
+    dout = rnd((B, S, H, D), 230 + seed)
+    out, lse = co.attention(q, k, v, scale)
+    dq, dk, dv = co.attention_bwd(q, k, v, dout, scale, lse, co.attention_delta(out, dout))
+    eps = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            keep = x[idx]
+            x[idx] = keep + eps
+            up = _loss(q, k, v, dout, scale)
+            x[idx] = keep - eps
+            dn = _loss(q, k, v, dout, scale)
+            x[idx] = keep
+            num[idx] = (up - dn) / (2 * eps)
+        np.testing.assert_allclose(g, num, atol=1e-8, rtol=1e-6)
+
+
+def test_bwd_matches_torch_autograd_float64():
+    torch = pytest.importorskip("torch")
+    B, S, H, D, scale = 2, 7, 3, 5, 0.4
+    q, k, v, dout = (rnd((B, S, H, D), 240 + i, 1.5) for i in range(4))
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    s = scale * torch.einsum("bihd,bjhd->bhij", tq, tk)
+    o = torch.einsum("bhij,bjhd->bihd", torch.softmax(s, dim=-1), tv)
+    o.backward(torch.tensor(dout, dtype=torch.float64))
+    dq, dk, dv = co.cp_attention_bwd(q, k, v, dout, scale)
+    for mine, ref in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+        np.testing.assert_allclose(mine, ref.numpy(), atol=1e-12, rtol=1e-10)
+
+
+def test_bwd_softmax_invariants():
+    # sum_j ds_ij = 0, so sum_j dk_j = 0; the weights sum to one per row, so
+    # sum_j dv_j = sum_i dout_i; and dq is unchanged when every key moves by
+    # the same vector (the logits of a row shift by one constant)
+    B, S, H, D, scale = 2, 9, 2, 4, 0.7
+    q, k, v, dout = (rnd((B, S, H, D), 250 + i) for i in range(4))
+    dq, dk, dv = co.cp_attention_bwd(q, k, v, dout, scale)
+    np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-12)
+    np.testing.assert_allclose(dv.sum(axis=1), dout.sum(axis=1), atol=1e-12)
+    shift = rnd((1, 1, H, D), 260)
+    dq2, _, _ = co.cp_attention_bwd(q, k + shift, v, dout, scale)
+    np.testing.assert_allclose(dq2, dq, atol=1e-12)
+
+
+def test_bwd_closed_forms():
+    # one key: out = v, so dv = sum of dout over the queries, dq = dk = 0
+    q, k, v, dout = rnd((1, 5, 2, 3), 270), rnd((1, 1, 2, 3), 271), rnd((1, 1, 2, 3), 272), rnd((1, 5, 2, 3), 273)
+    out, lse = co.attention(q, k, v, 0.5)
+    dq, dk, dv = co.attention_bwd(q, k, v, dout, 0.5, lse, co.attention_delta(out, dout))
+    np.testing.assert_allclose(dv[:, 0], dout.sum(axis=1), atol=1e-14)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-14)
+    np.testing.assert_allclose(dk, 0.0, atol=1e-14)
+    # q = 0: uniform weights 1/n, out = mean of v, so dv_j = sum_i dout_i / n and
+    # dq_i = scale * sum_j (dout_i . (v_j - mean v)) k_j / n; dk = 0 (q = 0)
+    n = 6
+    q = np.zeros((1, 4, 1, 3)); k, v, dout = rnd((1, n, 1, 3), 274), rnd((1, n, 1, 3), 275), rnd((1, 4, 1, 3), 276)
+    out, lse = co.attention(q, k, v, 0.9)
+    dq, dk, dv = co.attention_bwd(q, k, v, dout, 0.9, lse, co.attention_delta(out, dout))
+    np.testing.assert_allclose(dv[0, :, 0], np.tile(dout[0, :, 0].sum(axis=0) / n, (n, 1)), atol=1e-14)
+    vc = v[0, :, 0] - v[0, :, 0].mean(axis=0)
+    want = 0.9 * (dout[0, :, 0] @ vc.T) @ k[0, :, 0] / n
+    np.testing.assert_allclose(dq[0, :, 0], want, atol=1e-13)
+    np.testing.assert_allclose(dk, 0.0, atol=1e-14)
+
+
+@pytest.mark.parametrize("R,U,S,H", [(1, 1, 12, 4), (3, 1, 12, 4), (4, 1, 12, 2), (1, 2, 12, 4), (1, 4, 12, 4),
+                                     (2, 2, 12, 4), (3, 2, 12, 2)])
+def test_bwd_decompositions_equal_full_backward(R, U, S, H):
+    B, D, scale = 2, 3, 0.8
+    q, k, v, dout = (rnd((B, S, H, D), 280 + i, 1.3) for i in range(4))
+    out, lse = co.attention(q, k, v, scale)
+    full = co.attention_bwd(q, k, v, dout, scale, lse, co.attention_delta(out, dout))
+    got = co.cp_attention_bwd(q, k, v, dout, scale, R, U)
+    for a, b in zip(got, full):
+        np.testing.assert_allclose(a, b, atol=1e-12, rtol=0)
+
+
+def test_bwd_rejects_anything_and_uneven():
+    q = rnd((1, 7, 2, 2), 290)
+    with pytest.raises(co.UnsupportedComboError):
+        co.cp_attention_bwd(q, q, q, q, 0.5, 2, 1, True)
+    with pytest.raises(co.UnsupportedComboError):
+        co.cp_attention_bwd(q, q, q, q, 0.5, 1, 2, True)
+    with pytest.raises(co.NotDivisibleError):
+        co.cp_attention_bwd(q, q, q, q, 0.5, 2, 1, False)
+
+
+def _mut_bwd(kind):
+    def f(q, k, v, dout, scale, lse, delta):
+        q, k, v, dout, lse, delta = (co._f64(x) for x in (q, k, v, dout, lse, delta))
+        B, Sq, H, D = q.shape
+        dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+        for b in range(B):
+            for h in range(H):
+                qb, kb, vb, gb = q[b, :, h, :], k[b, :, h, :], v[b, :, h, :], dout[b, :, h, :]
+                s = scale * (qb @ kb.T)
+                p = np.exp(s - lse[b, h][:, None])
+                dv[b, :, h, :] = (p if kind == "dv_untransposed" else p.T) @ gb
+                dp = gb @ (kb if kind == "k_for_v" else vb).T
+                ds = p * (dp - (0.0 if kind == "no_delta" else delta[b, h][:, None]))
+                if kind == "ds_sign":
+                    ds = p * (delta[b, h][:, None] - dp)
+                dq[b, :, h, :] = (1.0 if kind == "dq_no_scale" else scale) * (ds @ kb)
+                dk[b, :, h, :] = scale * ((ds if kind == "dk_untransposed" else ds.T) @ qb)
+        return dq, dk, dv
+    return f
+
+
+@pytest.mark.parametrize("kind", ["no_delta", "ds_sign", "dq_no_scale", "k_for_v", "dk_untransposed",
+                                  "dv_untransposed"])
+def test_planted_bwd_mistakes_are_caught(kind):
+    # square blocks, so a transposed operand still has the right shape
+    B, S, H, D, scale = 1, 4, 1, 4, 0.6
+    q, k, v, dout = (rnd((B, S, H, D), 300 + i) for i in range(4))
+    out, lse = co.attention(q, k, v, scale)
+    got = _mut_bwd(kind)(q, k, v, dout, scale, lse, co.attention_delta(out, dout))
+    eps = 1e-6
+    worst = 0.0
+    for x, g in zip((q, k, v), got):
+        for idx in np.ndindex(*x.shape):
+            keep = x[idx]
+            x[idx] = keep + eps
+            up = _loss(q, k, v, dout, scale)
+            x[idx] = keep - eps
+            dn = _loss(q, k, v, dout, scale)
+            x[idx] = keep
+            worst = max(worst, abs(g[idx] - (up - dn) / (2 * eps)))
+    assert worst > 1e-4
+
+
+def test_planted_bwd_lap_mistake_is_caught():
+    # a lap whose blocks do not rotate (every rank sees its own block N times)
+    real = co.ring_shard_table
+    q, k, v, dout = (rnd((1, 8, 1, 2), 310 + i) for i in range(4))
+    full = co.cp_attention_bwd(q, k, v, dout, 0.5)
+    out, lse = co.attention(q, k, v, 0.5)
+    delta = co.attention_delta(out, dout)
+    table = real(8, 4, False)
+    dq = np.zeros(q.shape)
+    for r, (qo, ql) in enumerate(table):
+        for t in range(4):
+            ko, kl = table[r]  # the mistake: no rotation
+            gq, _, _ = co.attention_bwd(q[:, qo:qo + ql], k[:, ko:ko + kl], v[:, ko:ko + kl], dout[:, qo:qo + ql], 0.5,
+                                        lse[:, :, qo:qo + ql], delta[:, :, qo:qo + ql])
+            dq[:, qo:qo + ql] += gq
+    assert np.max(np.abs(dq - full[0])) > 1e-6
