@@ -1,10 +1,13 @@
-"""Context-parallel attention forward for diffusion transformers on one GB300.
+"""Context-parallel attention (forward and backward) for diffusion transformers on one GB300.
 
 The computation lives in libcpattn.so (hand-written CUDA for sm_103a, C ABI in
 include/cp_attn.h); this package is its build script and a thin torch binding.
 """
 from .api import (  # noqa: F401
     CpError,
+    cp_attention_bwd,
+    cp_attention_bwd_launch_count,
+    cp_attention_bwd_workspace_size,
     cp_attention_fwd,
     cp_attention_fwd_host,
     cp_attention_fwd_no_alloc,

@@ -52,6 +52,10 @@ SIGNATURES = {
                                      _vp]),
     "cp_attention_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz, _i, _i, _i,
                                    _vp]),
+    "cp_attention_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
+    "cp_attention_bwd_launch_count": (_i, [_i, _i, _i, _i, _i, _i, _i]),
+    "cp_attention_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz,
+                              _i, _vp]),
 }
 CP_NO_ALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
 

@@ -244,6 +244,48 @@ def cp_attention_fwd_no_alloc(q, k, v, out, lse, scale: float, ring_degree: int 
     check(st, "cp_attention_fwd_no_alloc")
 
 
+def cp_attention_bwd_workspace_size(B, H, S, D, ring_degree=1, ulysses_degree=1, dtype=torch.bfloat16) -> int:
+    return int(lib().cp_attention_bwd_workspace_size(B, H, S, D, ring_degree, ulysses_degree, _DT[dtype]))
+
+
+def cp_attention_bwd_launch_count(B, H, S, D, ring_degree=1, ulysses_degree=1, dtype=torch.bfloat16) -> int:
+    return int(lib().cp_attention_bwd_launch_count(B, H, S, D, ring_degree, ulysses_degree, _DT[dtype]))
+
+
+def cp_attention_bwd(q, k, v, out, dout, lse, dq, dk, dv, scale: float, ring_degree: int = 1,
+                     ulysses_degree: int = 1, uneven_ok: bool = False, workspace=None, stream=None):
+    """Backward of cp_attention_fwd: q, k, v, dout [B,S,H,D] (one dtype), out [B,S,H,D] f32 and
+    lse [B,H,S] f32 from the forward -> dq, dk, dv [B,S,H,D] f32 (written).
+
+    workspace: a CUDA uint8 tensor of at least cp_attention_bwd_workspace_size(...) bytes;
+    allocated here through torch when None.
+    """
+    _cuda(q, k, v, out, dout, lse, dq, dk, dv)
+    B, S, H, D = q.shape
+    for t in (k, v, dout, out, dq, dk, dv):
+        if t.shape != q.shape:
+            raise ValueError("shape mismatch")
+    if lse.shape != (B, H, S):
+        raise ValueError("lse must be [B, H, S]")
+    if k.dtype != q.dtype or v.dtype != q.dtype or dout.dtype != q.dtype:
+        raise TypeError("q, k, v and dout must share a dtype")
+    for t in (out, lse, dq, dk, dv):
+        if t.dtype != torch.float32:
+            raise TypeError("out, lse, dq, dk and dv must be float32")
+    for t in (q, k, v, out, dout, lse, dq, dk, dv):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be dense")
+    need = cp_attention_bwd_workspace_size(B, H, S, D, ring_degree, ulysses_degree, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _cuda(workspace)
+    st = lib().cp_attention_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
+                                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, D,
+                                float(scale), ring_degree, ulysses_degree, int(bool(uneven_ok)),
+                                workspace.data_ptr(), workspace.numel(), _dt(q), _stream(stream))
+    check(st, "cp_attention_bwd")
+
+
 def cp_check_device_status(stream=None) -> int:
     """Synchronizes the stream; returns 0, or CP_ERR_TIMEOUT if a kernel's bounded wait expired."""
     return int(lib().cp_check_device_status(_stream(stream)))
@@ -265,5 +307,6 @@ __all__ = [
     "CpError", "cp_block_attn_fwd", "cp_lse_merge", "cp_ulysses_seq2head", "cp_ulysses_head2seq",
     "cp_ulysses_anything_seq2head", "cp_ulysses_anything_head2seq",
     "cp_attention_validate", "cp_ring_shard_table", "cp_attention_workspace_size", "cp_attention_launch_count",
+    "cp_attention_bwd", "cp_attention_bwd_workspace_size", "cp_attention_bwd_launch_count",
     "cp_attention_fwd", "cp_attention_fwd_no_alloc", "cp_attention_fwd_host", "cp_attention_host_buffer_size", "cp_check_device_status", "cp_debug_bounded_wait_probe", "cp_status_string", "cp_version",
 ]

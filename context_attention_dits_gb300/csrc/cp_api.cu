@@ -841,3 +841,194 @@ extern "C" cp_status cp_attention_fwd_no_alloc(const void* q, const void* k, con
   return cp_attention_fwd(q, k, v, out, lse, B, H, S, D, scale, ring_degree, ulysses_degree, uneven_ok, ws,
                           CP_NO_ALLOC_WORKSPACE_BYTES, dt, mode, stream);
 }
+
+// ----------------------------------------------------------------------------
+// Backward (ring, Ulysses, unified; even splits only).
+// ----------------------------------------------------------------------------
+namespace {
+
+// Workspace layout of cp_attention_bwd (every piece 256-byte aligned):
+// delta [B, H, S]; with Ulysses, the head-group copies of q, k, v, dout
+// [U][B, S, H/U, D], of lse and delta [U][B, H/U, S], and the head-group
+// gradients dq, dk, dv [U][B, S, H/U, D] fp32.
+struct BwdWs {
+  size_t delta = 0, qh = 0, kh = 0, vh = 0, doh = 0, lh = 0, dlh = 0, dqh = 0, dkh = 0, dvh = 0, total = 0;
+};
+
+BwdWs bwd_ws_layout(int B, int H, int S, int D, int U, cp_dtype dt) {
+  BwdWs w;
+  const size_t n = static_cast<size_t>(B) * S * H * D, nl = static_cast<size_t>(B) * H * S;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = round_up(o + bytes, 256);
+    return at;
+  };
+  w.delta = take(nl * 4);
+  if (U > 1) {
+    w.qh = take(n * elem_size(dt));
+    w.kh = take(n * elem_size(dt));
+    w.vh = take(n * elem_size(dt));
+    w.doh = take(n * elem_size(dt));
+    w.lh = take(nl * 4);
+    w.dlh = take(nl * 4);
+    w.dqh = take(n * 4);
+    w.dkh = take(n * 4);
+    w.dvh = take(n * 4);
+  }
+  w.total = o;
+  return w;
+}
+
+cp_status bwd_validate(int B, int H, int S, int D, int R, int U, int uneven_ok, cp_dtype dt) {
+  // the Anything variants have no backward: Ring Anything is inference only
+  if (uneven_ok) return CP_ERR_UNSUPPORTED_COMBO;
+  return cp_attention_validate(B, H, S, D, R, U, 0, dt);
+}
+
+// Copies of the backward's Ulysses regroups: q, k, v, dout [B,S,H,D] -> [U][B,S,H/U,D]
+// and lse, delta [B,H,S] -> [U][B,H/U,S] (in), or dq, dk, dv back (out).
+void bwd_in_copies(const void* const src[4], void* const dst[4], const float* lse, const float* delta, float* lh,
+                   float* dlh, int B, int H, int S, int D, int U, int eb, std::vector<SegCopy>* cs) {
+  const int Hg = H / U;
+  const int64_t row = static_cast<int64_t>(Hg) * D;
+  for (int i = 0; i < 4; ++i)
+    cs->push_back(SegCopy{src[i], dst[i], 1, U, B, S, 0, row, static_cast<int64_t>(S) * H * D,
+                          static_cast<int64_t>(H) * D, row, eb});
+  // out segments (g, b, h) of S floats <- in[b, g*Hg + h, :]
+  const float* ls[2] = {lse, delta};
+  float* ld[2] = {lh, dlh};
+  for (int i = 0; i < 2; ++i)
+    cs->push_back(SegCopy{ls[i], ld[i], 1, U, B, Hg, 0, static_cast<int64_t>(Hg) * S, static_cast<int64_t>(H) * S,
+                          S, S, 4});
+}
+
+void bwd_out_copies(const float* const src[3], float* const dst[3], int B, int H, int S, int D, int U,
+                    std::vector<SegCopy>* cs) {
+  const int Hg = H / U;
+  const int64_t row = static_cast<int64_t>(Hg) * D, bstride = S * row;
+  for (int i = 0; i < 3; ++i)
+    cs->push_back(SegCopy{src[i], dst[i], 1, B, S, U, 0, bstride, row, static_cast<int64_t>(B) * bstride, row, 4});
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t cp_attention_bwd_workspace_size(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt) {
+  if (B < 0 || H < 1 || S < 0 || D < 1 || ring_degree < 1 || ulysses_degree < 1) return 0;
+  return bwd_ws_layout(B, H, S, D, ulysses_degree, dt).total;
+}
+
+int cp_attention_bwd_launch_count(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt) {
+  if (B <= 0 || S <= 0 || H < 1 || D < 1 || ring_degree < 1 || ulysses_degree < 1) return 0;
+  const int U = ulysses_degree;
+  int n = 3;  // delta, dq, dk/dv
+  if (U > 1 && H % U == 0) {
+    const BwdWs w = bwd_ws_layout(B, H, S, D, U, dt);
+    char* base = reinterpret_cast<char*>(uintptr_t{1} << 20);
+    const void* src[4] = {base, base, base, base};
+    void* dst[4] = {base + w.qh, base + w.kh, base + w.vh, base + w.doh};
+    std::vector<SegCopy> in, out;
+    bwd_in_copies(src, dst, reinterpret_cast<float*>(base), reinterpret_cast<float*>(base + w.delta),
+                  reinterpret_cast<float*>(base + w.lh), reinterpret_cast<float*>(base + w.dlh), B, H, S, D, U,
+                  elem_size(dt), &in);
+    const float* gs[3] = {reinterpret_cast<float*>(base + w.dqh), reinterpret_cast<float*>(base + w.dkh),
+                          reinterpret_cast<float*>(base + w.dvh)};
+    float* gd[3] = {reinterpret_cast<float*>(base), reinterpret_cast<float*>(base), reinterpret_cast<float*>(base)};
+    bwd_out_copies(gs, gd, B, H, S, D, U, &out);
+    n += cp::segment_copy_launches(in.data(), static_cast<int>(in.size())) +
+         cp::segment_copy_launches(out.data(), static_cast<int>(out.size()));
+  }
+  return n;
+}
+
+cp_status cp_attention_bwd(const void* q, const void* k, const void* v, const float* out, const void* dout,
+                           const float* lse, float* dq, float* dk, float* dv, int B, int H, int S, int D, float scale,
+                           int ring_degree, int ulysses_degree, int uneven_ok, void* workspace, size_t ws_bytes,
+                           cp_dtype dt, void* stream) {
+  cp_status st = bwd_validate(B, H, S, D, ring_degree, ulysses_degree, uneven_ok, dt);
+  if (st != CP_OK) return st;
+  if (!std::isfinite(scale)) return CP_ERR_INVALID_ARG;
+  if (B == 0 || S == 0) return CP_OK;
+  const void* ptrs[9] = {q, k, v, out, dout, lse, dq, dk, dv};
+  for (const void* p : ptrs) {
+    if (p == nullptr) return CP_ERR_INVALID_ARG;
+    if (!aligned16(p)) return CP_ERR_ALIGNMENT;
+  }
+  const int R = ring_degree, U = ulysses_degree;
+  const BwdWs w = bwd_ws_layout(B, H, S, D, U, dt);
+  if (!workspace || ws_bytes < w.total) return CP_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return CP_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev)) != CP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const bool bf16 = dt == CP_BF16;
+  float* delta = reinterpret_cast<float*>(ws + w.delta);
+  if (cp::launch_attn_bwd_delta(out, dout, delta, B, S, H, D, bf16, s) != cudaSuccess) return CP_ERR_CUDA;
+
+  cp::BwdArgs a{};
+  a.n = R;
+  if ((st = shard_table(S, R, false, a.off, a.len)) != CP_OK) return st;
+  a.q_prefix[0] = a.kv_prefix[0] = 0;
+  for (int r = 0; r < R; ++r) {
+    const int tiles = (a.len[r] + cp::kBwdTile - 1) / cp::kBwdTile;
+    a.q_prefix[r + 1] = a.q_prefix[r] + tiles;
+    a.kv_prefix[r + 1] = a.kv_prefix[r] + tiles;
+  }
+  a.S = S;
+  a.scale = scale;
+  if (U == 1) {
+    a.B = B;
+    a.H = H;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.dout = dout;
+    a.bstride = static_cast<int64_t>(S) * H * D;
+    a.sstride = static_cast<int64_t>(H) * D;
+    a.lse = lse;
+    a.delta = delta;
+    a.l_bstride = static_cast<int64_t>(H) * S;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    return cp::launch_attn_bwd(a, D, bf16, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+  }
+  // Ulysses / unified: regroup to head groups, the ring backward per group, regroup back
+  const int eb = elem_size(dt), Hg = H / U;
+  const void* src[4] = {q, k, v, dout};
+  void* dst[4] = {ws + w.qh, ws + w.kh, ws + w.vh, ws + w.doh};
+  float* lh = reinterpret_cast<float*>(ws + w.lh);
+  float* dlh = reinterpret_cast<float*>(ws + w.dlh);
+  std::vector<SegCopy> in;
+  bwd_in_copies(src, dst, lse, delta, lh, dlh, B, H, S, D, U, eb, &in);
+  if (cp::launch_segment_copies(in.data(), static_cast<int>(in.size()), s) != cudaSuccess) return CP_ERR_CUDA;
+  float* gq = reinterpret_cast<float*>(ws + w.dqh);
+  float* gk = reinterpret_cast<float*>(ws + w.dkh);
+  float* gv = reinterpret_cast<float*>(ws + w.dvh);
+  a.B = B * U;
+  a.H = Hg;
+  a.q = dst[0];
+  a.k = dst[1];
+  a.v = dst[2];
+  a.dout = dst[3];
+  a.bstride = static_cast<int64_t>(S) * Hg * D;
+  a.sstride = static_cast<int64_t>(Hg) * D;
+  a.lse = lh;
+  a.delta = dlh;
+  a.l_bstride = static_cast<int64_t>(Hg) * S;
+  a.dq = gq;
+  a.dk = gk;
+  a.dv = gv;
+  if (cp::launch_attn_bwd(a, D, bf16, s) != cudaSuccess) return CP_ERR_CUDA;
+  const float* gs[3] = {gq, gk, gv};
+  float* gd[3] = {dq, dk, dv};
+  std::vector<SegCopy> back;
+  bwd_out_copies(gs, gd, B, H, S, D, U, &back);
+  return cp::launch_segment_copies(back.data(), static_cast<int>(back.size()), s) == cudaSuccess ? CP_OK
+                                                                                               : CP_ERR_CUDA;
+}
+
+}  // extern "C"

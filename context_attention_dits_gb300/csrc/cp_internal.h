@@ -78,7 +78,38 @@ inline int tc_singles_for_rows(int rows) { return tc_tiles_for_rows(rows) % 2; }
 constexpr int kF32RowsPerCta = 8;
 inline int f32_items_for_rows(int rows) { return (rows + kF32RowsPerCta - 1) / kF32RowsPerCta; }
 
+// Backward of a ring lap over n even shards of one sequence (query shards and
+// K/V blocks share the table). q, k, v, dout and the outputs dq, dk, dv are
+// [B, S, H, D] with element strides (bstride, sstride, 1 per head of D);
+// lse and delta are [B, H, S] with batch stride l_bstride.
+constexpr int kBwdTile = 64;  // query rows per dq CTA, keys per dk/dv CTA
+struct BwdArgs {
+  int n;
+  int off[kMaxRanks];
+  int len[kMaxRanks];
+  int q_prefix[kMaxRanks + 1];   // dq CTAs per shard, prefix sums
+  int kv_prefix[kMaxRanks + 1];  // dk/dv CTAs per block, prefix sums
+  int B, H, S;
+  float scale;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dout;
+  int64_t bstride, sstride;
+  const float* lse;
+  const float* delta;
+  int64_t l_bstride;
+  float* dq;
+  float* dk;
+  float* dv;
+};
+
 // Launchers (each returns the launch error, cudaSuccess if none).
+// dq, then dk/dv, for D in {64, 128}; bf16 or fp32 inputs.
+cudaError_t launch_attn_bwd(const BwdArgs& a, int D, bool bf16, cudaStream_t s);
+// delta[b, h, s] = sum_d out[b, s, h, d] * dout[b, s, h, d] over dense [B, S, H, D].
+cudaError_t launch_attn_bwd_delta(const float* out, const void* dout, float* delta, int B, int S, int H, int D,
+                                  bool bf16, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t s);
 cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t s);

@@ -312,6 +312,48 @@ cp_status cp_attention_fwd_no_alloc(const void* q, const void* k, const void* v,
                                     int ring_degree, int ulysses_degree, int uneven_ok,
                                     cp_dtype dt, cp_lap_mode mode, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Backward (training): gradients of L = sum(out * dout) with respect to q, k
+ * and v for the attention cp_attention_fwd computes. The context parallelism
+ * page (variants table; Ring Attention, Ulysses Attention, Unified Attention
+ * sections) lets the plain variants serve training and marks Ring Anything
+ * as inference only; it gives no backward formulas. With
+ * p_ij = exp(scale q_i.k_j - lse_i) and delta_i = sum_d dout_id out_id:
+ *   dv_j = sum_i p_ij dout_i;  ds_ij = p_ij (dout_i.v_j - delta_i);
+ *   dq_i = scale sum_j ds_ij k_j;  dk_j = scale sum_i ds_ij q_i.
+ * The ring decomposition: each simulated rank's dq sums its lap's blocks in
+ * lap order ((r - t) mod R), and each block's dk, dv sum the ranks in the
+ * order the block visits them ((j + t) mod R), as dk, dv travel with K/V.
+ * -------------------------------------------------------------------------*/
+
+/* Bytes of device workspace cp_attention_bwd needs (256-byte aligned start):
+ * delta [B,H,S] fp32, and with ulysses_degree > 1 the head-group copies of
+ * q, k, v, dout, lse, delta and the head-group gradients. 0 for invalid sizes. */
+size_t cp_attention_bwd_workspace_size(int B, int H, int S, int D, int ring_degree, int ulysses_degree,
+                                       cp_dtype dt);
+
+/* Kernel launches one cp_attention_bwd call makes (delta, dq, dk/dv, and the
+ * Ulysses regroups). 0 for empty or invalid sizes. */
+int cp_attention_bwd_launch_count(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt);
+
+/* Backward of cp_attention_fwd (ring, Ulysses or unified).
+ *   q, k, v, dout : device [B, S, H, D] of dt (bf16 or fp32), dense;
+ *   out, lse      : the forward's results, fp32 [B, S, H, D] and [B, H, S];
+ *   dq, dk, dv    : device fp32 [B, S, H, D], written (not accumulated);
+ *   workspace     : device, >= cp_attention_bwd_workspace_size(...) bytes,
+ *                   256-byte aligned, owned by the caller.
+ * All arithmetic is fp32 (inputs widened on load). Asynchronous on `stream`.
+ * Errors (returned before any launch): the checks of cp_attention_validate
+ * with uneven_ok = 0; uneven_ok != 0 -> CP_ERR_UNSUPPORTED_COMBO (the
+ * Anything variants have no backward); a null pointer or non-finite scale ->
+ * CP_ERR_INVALID_ARG; a pointer not 16-byte aligned -> CP_ERR_ALIGNMENT;
+ * workspace missing or short -> CP_ERR_WORKSPACE; launch failure ->
+ * CP_ERR_CUDA. B == 0 or S == 0 returns CP_OK without launching. */
+cp_status cp_attention_bwd(const void* q, const void* k, const void* v, const float* out, const void* dout,
+                           const float* lse, float* dq, float* dk, float* dv, int B, int H, int S, int D,
+                           float scale, int ring_degree, int ulysses_degree, int uneven_ok, void* workspace,
+                           size_t ws_bytes, cp_dtype dt, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

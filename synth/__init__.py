@@ -11,8 +11,10 @@ Recipe (the same for every workload):
   * for bf16 workloads each tensor is then rounded to bfloat16 with
     round-to-nearest-even (``Tensor.to(torch.bfloat16)``);
   * the logit-stress variant multiplies ``q`` by 8 after rounding, which is
-    exact in bf16 (a power of two).
+    exact in bf16 (a power of two);
+  * a backward check draws ``dout`` N(0, 1) from its own generator
+    (seed + 1000), rounded like q, k, v.
 """
-from .workloads import WORKLOADS, Workload, make_qkv, make_merge_operands
+from .workloads import WORKLOADS, Workload, make_dout, make_merge_operands, make_qkv
 
-__all__ = ["WORKLOADS", "Workload", "make_qkv", "make_merge_operands"]
+__all__ = ["WORKLOADS", "Workload", "make_dout", "make_qkv", "make_merge_operands"]

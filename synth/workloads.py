@@ -88,6 +88,13 @@ def make_qkv(B: int, H: int, S: int, D: int, dtype: str, seed: int, q_mult: floa
     return q, k, v
 
 
+def make_dout(B: int, S: int, H: int, D: int, dtype: str, seed: int):
+    """The upstream gradient dout [B,S,H,D] of a backward check: float32 N(0, 1)
+    from its own CPU generator (seed + 1000), rounded to the workload dtype."""
+    g = torch.Generator().manual_seed(seed + 1000)
+    return torch.randn((B, S, H, D), generator=g, dtype=torch.float32).to(_torch_dtype(dtype))
+
+
 def make_merge_operands(B: int, H: int, S: int, D: int, seed: int, neg_inf_rows: int = 0):
     """Two fp32 (out, lse) partials of the shapes a ring step produces.
 

@@ -166,3 +166,32 @@ def test_masked_host_buffer_and_anything_entry_points_reject_before_launch():
     assert c(1, 24, 4481, 128, 1, 4, torch.bfloat16, "fused") == 4
     assert cpa.cp_attention_validate(1, 24, 4481, 128, 1, 4, True) == 0
     assert cpa.cp_attention_validate(1, 24, 4608, 128, 1, 5, True) == 0
+
+
+def test_bwd_sizes_counts_and_rejects_before_launch():
+    p = 1 << 20
+    L = _lib.lib()
+    n, nl = 4608 * 24 * 128, 24 * 4608
+    ws = cpa.cp_attention_bwd_workspace_size
+    assert ws(1, 24, 4608, 128, 4, 1, torch.bfloat16) >= nl * 4                      # delta only
+    assert ws(1, 24, 4608, 128, 1, 4, torch.bfloat16) >= nl * 4 + 4 * n * 2 + 2 * nl * 4 + 3 * n * 4
+    c = cpa.cp_attention_bwd_launch_count
+    assert c(1, 24, 4608, 128, 4, 1, torch.bfloat16) == 3       # delta, dq, dk/dv
+    # Ulysses: q, k, v, dout, lse, delta regroups share a launch, dq, dk, dv another
+    assert c(1, 24, 4608, 128, 1, 4, torch.bfloat16) == 5
+    assert c(0, 24, 4608, 128, 4, 1, torch.bfloat16) == 0
+    # q, k, v, out, dout, lse, dq, dk, dv, B, H, S, D, scale, R, U, ev, ws, ws_bytes, dt, stream
+    big = 1 << 34
+    f = lambda **kw: L.cp_attention_bwd(kw.get("q", p), p, p, p, p, p, p, p, kw.get("dv", p), 1, 24,
+                                        kw.get("S", 4608), kw.get("D", 128), kw.get("scale", 0.088), kw.get("R", 4),
+                                        kw.get("U", 1), kw.get("ev", 0), kw.get("ws", p), kw.get("wsb", big), 0, None)
+    assert f(ev=1, S=4607, R=3) == _lib.CP_ERR_UNSUPPORTED_COMBO   # Ring Anything: inference only
+    assert f(ev=1, U=4, R=1) == _lib.CP_ERR_UNSUPPORTED_COMBO
+    assert f(S=4607) == _lib.CP_ERR_NOT_DIVISIBLE
+    assert f(D=96) == _lib.CP_ERR_INVALID_ARG
+    assert f(scale=float("inf")) == _lib.CP_ERR_INVALID_ARG
+    assert f(q=0) == _lib.CP_ERR_INVALID_ARG
+    assert f(dv=p + 4) == _lib.CP_ERR_ALIGNMENT
+    assert f(ws=0) == _lib.CP_ERR_WORKSPACE
+    assert f(wsb=16) == _lib.CP_ERR_WORKSPACE
+    assert f(ws=p + 16) == _lib.CP_ERR_ALIGNMENT
