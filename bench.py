@@ -268,6 +268,27 @@ def secondary(cpa, dev, flush, stream, peaks):
     res["flux_ring4_text_padding_mask"] = {"TFLOP_s": tf, "ms": ms, "frac_of_bf16_peak": tf / bf16, "launches": 1,
                                            "note": "keys 300..511 masked; FLOPs counted as unmasked"}
     del q, k, v, out, lse, km
+
+    # backward of the FLUX ring-4 and Ulysses-4 forwards: algorithmic FLOPs are 2.5x the forward's
+    # (five S x S x D products per head: s recomputed, dp, dv, dq, dk); bf16 runs on the tensor cores
+    from synth import make_dout
+    for name, R, U in (("flux_ring4_bwd", 4, 1), ("flux_ulysses4_bwd", 1, 4)):
+        w = WORKLOADS["flux_ring4"]
+        q, k, v = (t.to(dev) for t in make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed))
+        dout = make_dout(w.B, w.S, w.H, w.D, w.dtype, w.seed).to(dev)
+        out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.float32, device=dev)
+        lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+        cpa.cp_attention_fwd(q, k, v, out, lse, w.scale, R, U, stream=stream)
+        grads = [torch.empty_like(out) for _ in range(3)]
+        ws = torch.empty(max(1, cpa.cp_attention_bwd_workspace_size(w.B, w.H, w.S, w.D, R, U, q.dtype)),
+                         dtype=torch.uint8, device=dev)
+        ms = _time_events(lambda: cpa.cp_attention_bwd(q, k, v, out, dout, lse, *grads, w.scale, R, U,
+                                                       workspace=ws, stream=stream), flush, stream, 3)
+        tf = 2.5 * w.flops / (ms * 1e-3) / 1e12
+        res[name] = {"TFLOP_s": tf, "ms": ms, "frac_of_bf16_peak": tf / bf16,
+                     "launches": cpa.cp_attention_bwd_launch_count(w.B, w.H, w.S, w.D, R, U, q.dtype),
+                     "note": "tensor-core backward, dq by fp32 atomics; FLOPs = 2.5 x forward"}
+        del q, k, v, dout, out, lse, grads, ws
     if cpa.cp_check_device_status() != 0:
         raise RuntimeError("device status after the secondary measurements")
     return res

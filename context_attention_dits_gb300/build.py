@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libcpattn.so")
-SOURCES = ["attn_tc.cu", "attn_bwd.cu", "kernels_simt.cu", "cp_api.cu"]
+SOURCES = ["attn_tc.cu", "attn_bwd.cu", "attn_bwd_tc.cu", "kernels_simt.cu", "cp_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

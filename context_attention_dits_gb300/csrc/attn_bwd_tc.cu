@@ -1,0 +1,439 @@
+// attn_bwd_tc.cu — backward of block / ring attention on the 5th-generation
+// tensor cores (tcgen05, bf16 operands, fp32 accumulators in tensor memory).
+//
+// The gradients are those of the CUDA-core backward (same formulas, same
+// ring walk; context parallelism page, Ring Attention section):
+//   p_ij = exp(scale q_i.k_j - lse_i),  ds_ij = p_ij (dout_i.v_j - delta_i),
+//   dv_j = sum_i p_ij dout_i,  dk_j = scale sum_i ds_ij q_i,  dq_i = scale sum_j ds_ij k_j.
+//
+// One CTA owns a tile of 128 keys of one (batch entry, head) and walks every
+// 128-row query tile of the lap, rank by rank in the order its K/V block
+// visits them ((j + t) mod n). Per query tile, five MMAs (M = 128):
+//   1. S^T  = K Q^T           (A = K tile, B = Q tile; both K-major)  -> TMEM [0, 128)
+//   2. dP^T = V dO^T          (A = V tile, B = dO tile)               -> TMEM [128, 256)
+//   3. dV  += P^T dO          (A = P^T in TMEM, B = dO MN-major)      -> TMEM [256, 256 + D)
+//   4. dK  += dS^T Q          (A = dS^T in TMEM, B = Q MN-major)      -> TMEM [256 + D, 256 + 2D)
+//   5. dQ   = dS K            (A = dS^T in shared memory read MN-major,
+//                              B = K tile MN-major)                   -> TMEM [128, 128 + D)
+// Between 2 and 3 the softmax warpgroup (one thread per key row) turns S^T
+// and dP^T into P^T (bf16, over S^T's first 64 columns) and dS^T (bf16, over
+// dP^T's first 64 columns, and into shared memory in the 128-byte-swizzled
+// layout that MMA 5 reads). A second warpgroup (one thread per query row)
+// drains each dQ tile and adds it into the fp32 dq in global memory with
+// 16-byte atomics; dq must start at zero. After the last query tile the
+// softmax warpgroup writes dk and dv once.
+//
+// Warp roles (320 threads): 0 = TMA producer (K, V once; Q, dO and the rows'
+// lse and delta per query tile, double-buffered), 1 = MMA issuer, 2-5 =
+// softmax, 6-9 = dQ drain. A warp reaches TMEM lanes 32 (warp mod 4) and up.
+// Every wait is bounded; on expiry the CTA records a timeout, lets its copies
+// land, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "cp_internal.h"
+#include "cp_ptx.cuh"
+
+namespace cp {
+namespace {
+
+constexpr int kThreadsB = 320;
+constexpr uint32_t kTmemColsB = 512;
+constexpr int kT = kBwdTcTile;  // keys per CTA, query rows per step
+constexpr float kLog2eB = 1.4426950408889634f;
+
+template <int D>
+struct BSmem {
+  static constexpr int kTile = kT * D * 2;   // one bf16 128-row tile
+  static constexpr int kHalf = kT * 128;     // one 64-column (128-byte) box of a 128-row tile
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kTile;
+  static constexpr int kOffQ = kOffV + kTile;      // two slots
+  static constexpr int kOffO = kOffQ + 2 * kTile;  // dO, two slots
+  static constexpr int kOffDS = kOffO + 2 * kTile; // dS^T: 128 key rows x 128 queries, two 64-query boxes
+  static constexpr int kOffLse = kOffDS + 2 * kHalf;  // two slots of 128 floats: lse * log2 e
+  static constexpr int kOffDlt = kOffLse + 2 * kT * 4; // two slots of 128 floats: delta
+  static constexpr int kOffBar = kOffDlt + 2 * kT * 4;
+  static constexpr int kNumBars = 11;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16;
+  // + room to align the base to 1024 bytes, as much as the 227 KB budget leaves
+  static constexpr int kMax = 227 * 1024;
+  static constexpr int kAlloc = kBytes + 1024 <= kMax ? kBytes + 1024 : kMax;
+};
+
+enum : int {
+  kBarKV = 0,      // K and V tiles landed
+  kBarQFull = 1,   // +slot: Q, dO, lse, delta of a query tile landed (TMA bytes + one arrive)
+  kBarQEmpty = 3,  // +slot: MMAs of the tile done with the slot
+  kBarSFull = 5,   // S^T and dP^T in TMEM
+  kBarPFull = 6,   // P^T, dS^T written (4 softmax warps arrive)
+  kBarDqFull = 7,  // dQ tile in TMEM
+  kBarDqEmpty = 8, // dQ tile read (4 drain warps arrive)
+  kBarDone = 9,    // every MMA of the CTA done: dK, dV final
+  kBarDrain = 10,
+};
+
+// Query tiles of the lap of K/V block jb, in the order the block visits the ranks.
+struct QCursor {
+  int t, tile, ntile, off, len;
+  __device__ __forceinline__ void init(const BwdArgs& a, int jb) {
+    t = -1;
+    next_block(a, jb);
+  }
+  __device__ __forceinline__ void next_block(const BwdArgs& a, int jb) {
+    tile = 0;
+    while (true) {
+      ++t;
+      if (t >= a.n) return;
+      const int r = (jb + t) % a.n;
+      off = a.off[r];
+      len = a.len[r];
+      ntile = (len + kT - 1) / kT;
+      if (ntile > 0) return;
+    }
+  }
+  __device__ __forceinline__ int q0() const { return off + tile * kT; }
+  __device__ __forceinline__ int nvalid() const { return min(kT, len - tile * kT); }
+  __device__ __forceinline__ void advance(const BwdArgs& a, int jb) {
+    if (++tile >= ntile) next_block(a, jb);
+  }
+};
+
+__device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1; !mbar_try_wait(bar, parity); ++n)
+    if ((n & 255u) == 0 && global_timer_ns() - t0 > timeout_ns) return;
+}
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                       const __grid_constant__ BwdArgs a) {
+  using L = BSmem<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzled tiles need a 1024-byte aligned base; with D = 128 the budget
+  // leaves less than 1024 bytes of slack, so a base that would need more is
+  // reported (uniformly, before any barrier or TMEM use) instead of used
+  const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+  if (pad > static_cast<uint32_t>(L::kAlloc - L::kBytes)) {
+    if (threadIdx.x == 0) atomicOr(a.err, kDevErrLayout);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = smem_addr(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);  // [0] TMEM base, [1] abort flag
+  volatile uint32_t* abort_flag = misc + 1;
+  auto bar = [&](int i) -> uint32_t { return sb + L::kOffBar + 8 * i; };
+  float* s_lse = reinterpret_cast<float*>(smem + L::kOffLse);
+  float* s_dlt = reinterpret_cast<float*>(smem + L::kOffDlt);
+
+  const int h = blockIdx.y, b = blockIdx.z;
+  int jb = 0;
+  while (jb + 1 < a.n && a.kv_prefix[jb + 1] <= static_cast<int>(blockIdx.x)) ++jb;
+  const int key0 = a.off[jb] + (static_cast<int>(blockIdx.x) - a.kv_prefix[jb]) * kT;
+  const int nk = min(kT, a.off[jb] + a.len[jb] - key0);
+  int NQT = 0;
+  for (int t = 0; t < a.n; ++t) NQT += (a.len[(jb + t) % a.n] + kT - 1) / kT;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::kNumBars; ++i) {
+      const bool two = i == kBarQFull || i == kBarQFull + 1;
+      const bool four = i == kBarPFull || i == kBarDqEmpty;
+      mbar_init(bar(i), two ? 2 : (four ? 4 : 1));
+    }
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(misc), kTmemColsB);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const uint64_t tmo = a.timeout_ns;
+
+  if (warp == 0) {
+    // ===================== TMA producer =====================
+    const bool leader = elect_one();
+    if (leader) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&to);
+      mbar_arrive_expect_tx(bar(kBarKV), 2 * L::kTile);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_4d(sb + L::kOffK + c * L::kHalf, &tk, bar(kBarKV), c * 64, h, key0, b);
+        tma_load_4d(sb + L::kOffV + c * L::kHalf, &tv, bar(kBarKV), c * 64, h, key0, b);
+      }
+    }
+    int issued[2] = {0, 0};
+    QCursor cur;
+    cur.init(a, jb);
+    for (int it = 0; it < NQT; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarQEmpty + s), ph ^ 1, abort_flag, a.err, tmo))) break;
+      const int q0 = cur.q0(), nq = cur.nvalid();
+      if (leader) {
+        mbar_arrive_expect_tx(bar(kBarQFull + s), 2 * L::kTile);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(sb + L::kOffQ + s * L::kTile + c * L::kHalf, &tq, bar(kBarQFull + s), c * 64, h, q0, b);
+          tma_load_4d(sb + L::kOffO + s * L::kTile + c * L::kHalf, &to, bar(kBarQFull + s), c * 64, h, q0, b);
+        }
+      }
+      // the rows' lse (times log2 e) and delta; rows past the tile, and rows
+      // that saw no key, get lse = +inf so that p = 0
+      for (int i = lane; i < kT; i += 32) {
+        float l = INFINITY, dl = 0.f;
+        if (i < nq) {
+          const int64_t o = b * a.l_bstride + static_cast<int64_t>(h) * a.S + q0 + i;
+          l = a.lse[o];
+          l = l == -INFINITY ? INFINITY : l * kLog2eB;
+          dl = a.delta[o];
+        }
+        s_lse[s * kT + i] = l;
+        s_dlt[s * kT + i] = dl;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarQFull + s));
+      ++issued[s];
+      cur.advance(a, jb);
+    }
+    if (*abort_flag) {
+      // let every issued copy land before the CTA's shared memory goes away
+      drain_wait_b(bar(kBarKV), 0, tmo);
+      for (int s = 0; s < 2; ++s)
+        if (issued[s]) drain_wait_b(bar(kBarQFull + s), (issued[s] - 1) & 1, tmo);
+    }
+  } else if (warp == 1) {
+    // ===================== MMA issuer =====================
+    const bool leader = elect_one();
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kT, kT, false, false);  // S^T, dP^T: M = keys, N = queries
+    constexpr uint32_t idesc_g = idesc_bf16_f32(kT, D, false, true);    // dV, dK: A in TMEM, B MN-major
+    constexpr uint32_t idesc_q = idesc_bf16_f32(kT, D, true, true);     // dQ: A and B MN-major
+    const uint64_t k_km = smem_desc_sw128(sb + L::kOffK, 16, 1024);
+    const uint64_t v_km = smem_desc_sw128(sb + L::kOffV, 16, 1024);
+    const uint64_t q_km = smem_desc_sw128(sb + L::kOffQ, 16, 1024);
+    const uint64_t o_km = smem_desc_sw128(sb + L::kOffO, 16, 1024);
+    const uint64_t q_mn = smem_desc_sw128(sb + L::kOffQ, L::kHalf, 1024);
+    const uint64_t o_mn = smem_desc_sw128(sb + L::kOffO, L::kHalf, 1024);
+    const uint64_t k_mn = smem_desc_sw128(sb + L::kOffK, L::kHalf, 1024);
+    const uint64_t ds_mn = smem_desc_sw128(sb + L::kOffDS, L::kHalf, 1024);
+    const uint32_t km_hi = static_cast<uint32_t>(k_km >> 32), mn_hi = static_cast<uint32_t>(k_mn >> 32);
+    const uint32_t k_km_lo = static_cast<uint32_t>(k_km), v_km_lo = static_cast<uint32_t>(v_km);
+    const uint32_t q_km_lo = static_cast<uint32_t>(q_km), o_km_lo = static_cast<uint32_t>(o_km);
+    const uint32_t q_mn_lo = static_cast<uint32_t>(q_mn), o_mn_lo = static_cast<uint32_t>(o_mn);
+    const uint32_t k_mn_lo = static_cast<uint32_t>(k_mn), ds_mn_lo = static_cast<uint32_t>(ds_mn);
+    auto commit = [&](uint32_t bar_addr) {
+      if (leader) mma_commit(bar_addr);
+    };
+    // K-major operands: 16-element K steps within a 64-column box, then the next box
+    auto kstep = [](int kk) -> uint32_t { return static_cast<uint32_t>(((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4); };
+    bool ok = mbar_wait_bounded(bar(kBarKV), 0, abort_flag, a.err, tmo);
+    for (int it = 0; ok && it < NQT; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      const uint32_t slot = static_cast<uint32_t>((s * L::kTile) >> 4);
+      if (!mbar_wait_bounded(bar(kBarQFull + s), ph, abort_flag, a.err, tmo)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // 1. S^T = K Q^T
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        if (leader) mma_ss_lohi(tmem, k_km_lo + kstep(kk), km_hi, q_km_lo + slot + kstep(kk), km_hi, idesc_s, kk > 0);
+      // 2. dP^T = V dO^T, once the previous dQ tile has left its columns
+      if (it > 0 && !mbar_wait_bounded(bar(kBarDqEmpty), (it - 1) & 1, abort_flag, a.err, tmo)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        if (leader)
+          mma_ss_lohi(tmem + 128, v_km_lo + kstep(kk), km_hi, o_km_lo + slot + kstep(kk), km_hi, idesc_s, kk > 0);
+      commit(bar(kBarSFull));
+      if (!mbar_wait_bounded(bar(kBarPFull), it & 1, abort_flag, a.err, tmo)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // 3. dV += P^T dO;  4. dK += dS^T Q   (K = query rows: 16 rows = 2048 bytes of an MN-major tile)
+#pragma unroll
+      for (int kk = 0; kk < kT / 16; ++kk)
+        if (leader) mma_ts_lohi(tmem + 256, tmem + kk * 8, o_mn_lo + slot + ((kk * 2048) >> 4), mn_hi, idesc_g,
+                                (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < kT / 16; ++kk)
+        if (leader) mma_ts_lohi(tmem + 256 + D, tmem + 128 + kk * 8, q_mn_lo + slot + ((kk * 2048) >> 4), mn_hi,
+                                idesc_g, (it > 0 || kk > 0) ? 1u : 0u);
+      // 5. dQ = dS K   (K = keys: 16 key rows = 2048 bytes of both MN-major tiles)
+#pragma unroll
+      for (int kk = 0; kk < kT / 16; ++kk)
+        if (leader) mma_ss_lohi(tmem + 128, ds_mn_lo + ((kk * 2048) >> 4), mn_hi, k_mn_lo + ((kk * 2048) >> 4), mn_hi,
+                                idesc_q, kk > 0);
+      commit(bar(kBarDqFull));
+      commit(bar(kBarQEmpty + s));
+    }
+    if (ok) {
+      commit(bar(kBarDone));
+    } else {
+      commit(bar(kBarDrain));
+      drain_wait_b(bar(kBarDrain), 0, tmo);
+    }
+  } else if (warp < 6) {
+    // ===================== softmax: one thread per key row =====================
+    const int wq = warp & 3;
+    const int key = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
+    const bool kvalid = key < nk;
+    const float c2 = a.scale * kLog2eB;
+    uint8_t* ds_row = smem + L::kOffDS + key * 128;
+    bool ok = true;
+    for (int it = 0; it < NQT; ++it) {
+      const int s = it & 1;
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait_bounded(bar(kBarQFull + s), (it >> 1) & 1, abort_flag, a.err, tmo) &&
+                          mbar_wait_bounded(bar(kBarSFull), it & 1, abort_flag, a.err, tmo));
+      if (!ok) break;
+      tc_fence_after();
+      const float* lse2 = s_lse + s * kT;
+      const float* dlt = s_dlt + s * kT;
+#pragma unroll 1
+      for (int c = 0; c < kT / 32; ++c) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(t_s + c * 32, sr);
+        tmem_ld32(t_dp + c * 32, dr);
+        tmem_wait_ld();
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const int q = c * 32 + 2 * x;
+          float p0 = exp2f(fmaf(u2f(sr[2 * x]), c2, -lse2[q]));
+          float p1 = exp2f(fmaf(u2f(sr[2 * x + 1]), c2, -lse2[q + 1]));
+          p0 = kvalid ? p0 : 0.f;
+          p1 = kvalid ? p1 : 0.f;
+          const float d0 = p0 * (u2f(dr[2 * x]) - dlt[q]);
+          const float d1 = p1 * (u2f(dr[2 * x + 1]) - dlt[q + 1]);
+          pp[x] = pack_bf16x2(p0, p1);
+          dd[x] = pack_bf16x2(d0, d1);
+        }
+        // P^T over S^T's consumed columns, dS^T over dP^T's consumed columns
+        tmem_st16(t_s + c * 16, pp);
+        tmem_st16(t_dp + c * 16, dd);
+        // dS^T row `key`, queries c*32 .. c*32+31: box c/2, 16-byte units (c%2)*4 .. +3, 128-byte swizzle
+        uint8_t* box = ds_row + (c >> 1) * L::kHalf;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = (c & 1) * 4 + u;
+          *reinterpret_cast<uint4*>(box + ((unit ^ (key & 7)) << 4)) =
+              make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarPFull));
+    }
+    // ---- dk, dv of this CTA's keys ----
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarDone), 0, abort_flag, a.err, tmo));
+    if (ok) {
+      tc_fence_after();
+      const int64_t o = b * a.bstride + static_cast<int64_t>(key0 + key) * a.sstride + h * D;
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {
+        float* dst = g == 0 ? a.dv : a.dk;
+        const float mul = g == 0 ? 1.f : a.scale;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + 256 + g * D + c * 32, r);
+          tmem_wait_ld();
+          if (kvalid) {
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+              *reinterpret_cast<float4*>(dst + o + c * 32 + x) =
+                  make_float4(u2f(r[x]) * mul, u2f(r[x + 1]) * mul, u2f(r[x + 2]) * mul, u2f(r[x + 3]) * mul);
+          }
+        }
+      }
+    }
+  } else {
+    // ===================== dQ drain: one thread per query row =====================
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t t_q = tmem + (static_cast<uint32_t>(wq * 32) << 16) + 128;
+    QCursor cur;
+    cur.init(a, jb);
+    for (int it = 0; it < NQT; ++it) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarDqFull), it & 1, abort_flag, a.err, tmo))) break;
+      tc_fence_after();
+      uint32_t r[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(t_q + c * 32, r[c]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarDqEmpty));
+      if (row < cur.nvalid()) {
+        float* dst = a.dq + b * a.bstride + static_cast<int64_t>(cur.q0() + row) * a.sstride + h * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int x = 0; x < 32; x += 4)
+            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + x),
+                      make_float4(u2f(r[c][x]) * a.scale, u2f(r[c][x + 1]) * a.scale, u2f(r[c][x + 2]) * a.scale,
+                                  u2f(r[c][x + 3]) * a.scale));
+      }
+      cur.advance(a, jb);
+    }
+  }
+
+  // ---- teardown: every thread of the CTA arrives here, aborted or not ----
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemColsB);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_tc_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& to, cudaStream_t s) {
+  using L = BSmem<D>;
+  static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int tiles = a.kv_prefix[a.n];
+  if (tiles == 0 || a.H == 0 || a.B == 0) return cudaSuccess;
+  attn_bwd_tc_kernel<D><<<dim3(tiles, a.H, a.B), kThreadsB, L::kAlloc, s>>>(tq, tk, tv, to, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_tc(const BwdArgs& a, int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t s) {
+  if (D == 128) return launch_bwd_tc_d<128>(a, tq, tk, tv, to, s);
+  if (D == 64) return launch_bwd_tc_d<64>(a, tq, tk, tv, to, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cp

@@ -780,7 +780,8 @@ cp_status cp_check_device_status(void* stream) {
   if (cudaMemcpy(&word, dev->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return CP_ERR_CUDA;
   if (word == 0) return CP_OK;
   if (cudaMemset(dev->err, 0, sizeof(word)) != cudaSuccess) return CP_ERR_CUDA;
-  return CP_ERR_TIMEOUT;
+  // bit 0: a bounded wait expired; bit 1: a kernel found its shared memory misaligned
+  return (word & 1u) ? CP_ERR_TIMEOUT : CP_ERR_CUDA;
 }
 
 cp_status cp_debug_bounded_wait_probe(int timeout_us, void* stream) {
@@ -923,7 +924,7 @@ size_t cp_attention_bwd_workspace_size(int B, int H, int S, int D, int ring_degr
 int cp_attention_bwd_launch_count(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt) {
   if (B <= 0 || S <= 0 || H < 1 || D < 1 || ring_degree < 1 || ulysses_degree < 1) return 0;
   const int U = ulysses_degree;
-  int n = 3;  // delta, dq, dk/dv
+  int n = dt == CP_BF16 ? 2 : 3;  // delta, then the tensor-core kernel, or the dq and dk/dv kernels
   if (U > 1 && H % U == 0) {
     const BwdWs w = bwd_ws_layout(B, H, S, D, U, dt);
     char* base = reinterpret_cast<char*>(uintptr_t{1} << 20);
@@ -966,19 +967,37 @@ cp_status cp_attention_bwd(const void* q, const void* k, const void* v, const fl
   char* ws = static_cast<char*>(workspace);
   const bool bf16 = dt == CP_BF16;
   float* delta = reinterpret_cast<float*>(ws + w.delta);
-  if (cp::launch_attn_bwd_delta(out, dout, delta, B, S, H, D, bf16, s) != cudaSuccess) return CP_ERR_CUDA;
+  // the tensor-core kernel accumulates dq with atomics: the delta launch zeroes it
+  float* dq_acc = U > 1 ? reinterpret_cast<float*>(ws + w.dqh) : dq;
+  if (cp::launch_attn_bwd_delta(out, dout, delta, bf16 ? dq_acc : nullptr, B, S, H, D, bf16, s) != cudaSuccess)
+    return CP_ERR_CUDA;
 
   cp::BwdArgs a{};
   a.n = R;
   if ((st = shard_table(S, R, false, a.off, a.len)) != CP_OK) return st;
   a.q_prefix[0] = a.kv_prefix[0] = 0;
+  const int tile = bf16 ? cp::kBwdTcTile : cp::kBwdTile;
   for (int r = 0; r < R; ++r) {
-    const int tiles = (a.len[r] + cp::kBwdTile - 1) / cp::kBwdTile;
+    const int tiles = (a.len[r] + tile - 1) / tile;
     a.q_prefix[r + 1] = a.q_prefix[r] + tiles;
     a.kv_prefix[r + 1] = a.kv_prefix[r] + tiles;
   }
   a.S = S;
   a.scale = scale;
+  a.err = dev->err;
+  a.timeout_ns = kWaitTimeoutNs;
+  // bf16: tensor maps over the (possibly head-grouped) q, k, v, dout, then the tensor-core kernel
+  auto run = [&](int Bn, int Hx) -> cp_status {
+    if (!bf16) return cp::launch_attn_bwd(a, D, false, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+    CUtensorMap tq, tk, tv, to;
+    const int64_t row = static_cast<int64_t>(Hx) * D;
+    if (!make_tmap_bf16(&tq, a.q, D, Hx, S, Bn, row, a.bstride) ||
+        !make_tmap_bf16(&tk, a.k, D, Hx, S, Bn, row, a.bstride) ||
+        !make_tmap_bf16(&tv, a.v, D, Hx, S, Bn, row, a.bstride) ||
+        !make_tmap_bf16(&to, a.dout, D, Hx, S, Bn, row, a.bstride))
+      return CP_ERR_CUDA;
+    return cp::launch_attn_bwd_tc(a, D, tq, tk, tv, to, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+  };
   if (U == 1) {
     a.B = B;
     a.H = H;
@@ -994,7 +1013,7 @@ cp_status cp_attention_bwd(const void* q, const void* k, const void* v, const fl
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
-    return cp::launch_attn_bwd(a, D, bf16, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+    return run(B, H);
   }
   // Ulysses / unified: regroup to head groups, the ring backward per group, regroup back
   const int eb = elem_size(dt), Hg = H / U;
@@ -1022,7 +1041,7 @@ cp_status cp_attention_bwd(const void* q, const void* k, const void* v, const fl
   a.dq = gq;
   a.dk = gk;
   a.dv = gv;
-  if (cp::launch_attn_bwd(a, D, bf16, s) != cudaSuccess) return CP_ERR_CUDA;
+  if ((st = run(B * U, Hg)) != CP_OK) return st;
   const float* gs[3] = {gq, gk, gv};
   float* gd[3] = {dq, dk, dv};
   std::vector<SegCopy> back;

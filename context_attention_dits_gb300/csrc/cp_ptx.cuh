@@ -62,7 +62,7 @@ __device__ __forceinline__ bool elect_one() {
 }
 
 // Error codes recorded in the device error word.
-enum : uint32_t { kDevErrTimeout = 1u };
+enum : uint32_t { kDevErrTimeout = 1u, kDevErrLayout = 2u };
 
 // Bounded wait for the phase of `bar` with the given parity to complete.
 // Returns true on completion. Returns false when another role of the CTA has
@@ -212,6 +212,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 #undef CP_W8
+
+#define CP_W4(i) "r"(r[i + 0]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3])
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      CP_W4(0), CP_W4(4), CP_W4(8), CP_W4(12)
+      : "memory");
+}
+#undef CP_W4
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tensor-core operand reads through a matrix descriptor).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }

@@ -272,8 +272,10 @@ cp_status cp_attention_fwd_host(const void* q, const void* k, const void* v, flo
 
 /*
  * Synchronizes stream, then reads and clears the device error word on the
- * current device. Returns CP_OK if no kernel reported an expired wait since
- * the last call, CP_ERR_TIMEOUT if one did, CP_ERR_CUDA if the read failed.
+ * current device. Returns CP_OK if no kernel reported a problem since the
+ * last call, CP_ERR_TIMEOUT if a kernel's bounded wait expired, CP_ERR_CUDA
+ * if a kernel found its shared memory base misaligned (it then did no work)
+ * or the read failed.
  */
 cp_status cp_check_device_status(void* stream);
 
@@ -342,7 +344,10 @@ int cp_attention_bwd_launch_count(int B, int H, int S, int D, int ring_degree, i
  *   dq, dk, dv    : device fp32 [B, S, H, D], written (not accumulated);
  *   workspace     : device, >= cp_attention_bwd_workspace_size(...) bytes,
  *                   256-byte aligned, owned by the caller.
- * All arithmetic is fp32 (inputs widened on load). Asynchronous on `stream`.
+ * bf16 runs on the tensor cores: bf16 operands (P and dS rounded to bf16
+ * for their products), fp32 accumulation, dq accumulated with fp32 atomics
+ * (its summation order varies from run to run). fp32 runs on the CUDA cores
+ * in fp32 throughout. Asynchronous on `stream`.
  * Errors (returned before any launch): the checks of cp_attention_validate
  * with uneven_ok = 0; uneven_ok != 0 -> CP_ERR_UNSUPPORTED_COMBO (the
  * Anything variants have no backward); a null pointer or non-finite scale ->

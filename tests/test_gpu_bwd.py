@@ -1,11 +1,10 @@
 """GPU parity of the backward (cp_attention_bwd) against the float64 oracle.
 
 Both sides take the same forward results (out, lse): the oracle's, rounded to
-fp32, so the check isolates the backward's arithmetic. The kernels compute in
-fp32 (bf16 inputs widened on load), so the bound is the fp32 one derived for
-the CUDA-core forward, loosened for the longer sums of the backward
-(dq_i sums S products, each carrying an exp and two D-term dot products):
-relative L2 <= 1e-4 and max abs <= 1e-3 x max |reference| per gradient.
+fp32, so the check isolates the backward's arithmetic. fp32 inputs run on the
+CUDA cores in fp32: relative L2 <= 1e-4 and max abs <= 1e-3 x max |reference|
+(the fp32 forward's bound, loosened for the longer sums of the backward).
+bf16 inputs run on the tensor cores: the forward's bf16 bounds (see TOL).
 """
 import numpy as np
 import pytest
@@ -16,8 +15,13 @@ from synth import make_dout, make_qkv
 
 pytestmark = pytest.mark.gpu
 
-REL_L2 = 1e-4
-MAX_ABS_REL = 1e-3
+# (relative L2, max abs as a fraction of max |reference|) per input dtype. bf16
+# runs on the tensor cores with P and dS rounded to bf16 (relative 2^-9) for
+# their products: measured ~1.7e-3 relative L2 on random inputs, so the
+# forward's bf16 bounds (5e-3 relative L2, 1e-2 max abs at unit scale) apply,
+# the max abs taken relative to the gradient's largest entry.
+TOL = {"f32": (1e-4, 1e-3), "bf16": (5e-3, 1e-2)}
+ZERO_ABS = 1e-4  # where the exact gradient is 0 (one key), only this absolute bound
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -33,16 +37,22 @@ def cpa():
     return m
 
 
-def check(got, want, what):
+def check(got, want, what, dtype):
+    rel_tol, abs_tol = TOL[dtype]
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert got.shape == want.shape, what
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     err = np.abs(got - want)
-    scale = max(float(np.abs(want).max()), 1e-30)
+    if float(np.abs(want).max()) == 0.0:
+        print(f"{what}: exact zero, max abs {err.max():.3e}")
+        assert err.max() <= ZERO_ABS, f"{what}: max abs {err.max():.3e} > {ZERO_ABS} where the gradient is 0"
+        return
+    scale = float(np.abs(want).max())
     rl = float(np.sqrt(np.sum((got - want) ** 2)) / max(np.sqrt(np.sum(want * want)), 1e-300))
-    assert err.max() <= MAX_ABS_REL * scale, f"{what}: max abs {err.max():.3e} > {MAX_ABS_REL} x {scale:.3e}"
-    assert rl <= REL_L2, f"{what}: rel L2 {rl:.3e} > {REL_L2}"
+    print(f"{what}: rel L2 {rl:.3e}, max abs / max ref {err.max() / scale:.3e}")
+    assert err.max() <= abs_tol * scale, f"{what}: max abs {err.max():.3e} > {abs_tol} x {scale:.3e}"
+    assert rl <= rel_tol, f"{what}: rel L2 {rl:.3e} > {rel_tol}"
 
 
 def run_bwd(q, k, v, out, dout, lse, scale, R, U):
@@ -71,7 +81,7 @@ def test_bwd_matches_oracle(B, S, H, D, R, U, dtype):
     want = co.cp_attention_bwd(q, k, v, dout, scale, R, U, out=out32.double().numpy(), lse=lse32.double().numpy())
     got = run_bwd(q, k, v, out32, dout, lse32, scale, R, U)
     for name, g, w in zip(("dq", "dk", "dv"), got, want):
-        check(g, w, f"{name} B{B} S{S} H{H} D{D} R{R} U{U} {dtype}")
+        check(g, w, f"{name} B{B} S{S} H{H} D{D} R{R} U{U} {dtype}", dtype)
 
 
 def test_bwd_flux_ring4_sampled():
@@ -104,9 +114,9 @@ def test_bwd_flux_ring4_sampled():
     gq, _, _ = co.attention_bwd(sub[0][:, idx], sub[1], sub[2], sub[3][:, idx], scale, l64[:, :, idx],
                                 delta[:, :, idx])
     _, gk, gv = co.attention_bwd(sub[0], sub[1][:, idx], sub[2][:, idx], sub[3], scale, l64, delta)
-    check(dq[:, idx], gq, "dq sampled rows")
-    check(dk[:, idx], gk, "dk sampled keys")
-    check(dv[:, idx], gv, "dv sampled keys")
+    check(dq[:, idx], gq, "dq sampled rows", "bf16")
+    check(dk[:, idx], gk, "dk sampled keys", "bf16")
+    check(dv[:, idx], gv, "dv sampled keys", "bf16")
 
 
 def test_bwd_rejects_anything_variants():
