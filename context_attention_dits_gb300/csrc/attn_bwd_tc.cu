@@ -320,17 +320,30 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tmem_ld32(t_dp + c * 32, dr);
         tmem_wait_ld();
         uint32_t pp[16], dd[16];
+        if (kvalid) {
+          // p = 2^(s c2 - lse2) (lse2 = +inf past the tile: p = 0), ds = p (dp - delta); pairs of
+          // columns in packed fp32x2 FMAs, lse and delta read as 16-byte vectors
+          const float4* l4 = reinterpret_cast<const float4*>(lse2 + c * 32);
+          const float4* d4 = reinterpret_cast<const float4*>(dlt + c * 32);
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int q = c * 32 + 2 * x;
-          float p0 = exp2f(fmaf(u2f(sr[2 * x]), c2, -lse2[q]));
-          float p1 = exp2f(fmaf(u2f(sr[2 * x + 1]), c2, -lse2[q + 1]));
-          p0 = kvalid ? p0 : 0.f;
-          p1 = kvalid ? p1 : 0.f;
-          const float d0 = p0 * (u2f(dr[2 * x]) - dlt[q]);
-          const float d1 = p1 * (u2f(dr[2 * x + 1]) - dlt[q + 1]);
-          pp[x] = pack_bf16x2(p0, p1);
-          dd[x] = pack_bf16x2(d0, d1);
+          for (int x = 0; x < 8; ++x) {
+            const float4 lv = l4[x], dv4 = d4[x];
+            const float nl[4] = {-lv.x, -lv.y, -lv.z, -lv.w}, nd[4] = {-dv4.x, -dv4.y, -dv4.z, -dv4.w};
+#pragma unroll
+            for (int y = 0; y < 4; y += 2) {
+              const int e = 4 * x + y;
+              float t0, t1, g0, g1, d0, d1;
+              fma2(t0, t1, u2f(sr[e]), u2f(sr[e + 1]), c2, c2, nl[y], nl[y + 1]);
+              fma2(g0, g1, u2f(dr[e]), u2f(dr[e + 1]), 1.f, 1.f, nd[y], nd[y + 1]);
+              const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+              fma2(d0, d1, p0, p1, g0, g1, 0.f, 0.f);
+              pp[e >> 1] = pack_bf16x2(p0, p1);
+              dd[e >> 1] = pack_bf16x2(d0, d1);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) pp[x] = dd[x] = 0u;  // a key past the tile: p = ds = 0
         }
         // P^T over S^T's consumed columns, dS^T over dP^T's consumed columns
         tmem_st16(t_s + c * 16, pp);

@@ -284,6 +284,16 @@ __device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float 
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
 
+// (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1) in one packed fp32x2 FMA (sm_100+).
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                     float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // s0 += low bf16 of pk, s1 += high bf16 of pk (mixed-precision adds, sm_100+).
 __device__ __forceinline__ void add_bf16x2_to_f32(float& s0, float& s1, uint32_t pk) {
   asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
