@@ -41,7 +41,7 @@
 namespace cp {
 namespace {
 
-constexpr int kThreadsB = 320;
+constexpr int kThreadsB = 192;
 constexpr uint32_t kTmemColsB = 512;
 constexpr int kT = kBwdTcTile;  // keys per CTA, query rows per step
 constexpr float kLog2eB = 1.4426950408889634f;
@@ -54,11 +54,10 @@ struct BSmem {
   static constexpr int kOffV = kOffK + kTile;
   static constexpr int kOffQ = kOffV + kTile;      // two slots
   static constexpr int kOffO = kOffQ + 2 * kTile;  // dO, two slots
-  static constexpr int kOffDS = kOffO + 2 * kTile; // dS^T: 128 key rows x 128 queries, two 64-query boxes
-  static constexpr int kOffLse = kOffDS + 2 * kHalf;  // two slots of 128 floats: lse * log2 e
+  static constexpr int kOffLse = kOffO + 2 * kTile;   // two slots of 128 floats: lse * log2 e
   static constexpr int kOffDlt = kOffLse + 2 * kT * 4; // two slots of 128 floats: delta
   static constexpr int kOffBar = kOffDlt + 2 * kT * 4;
-  static constexpr int kNumBars = 11;
+  static constexpr int kNumBars = 9;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   // + room to align the base to 1024 bytes, as much as the 227 KB budget leaves
@@ -72,10 +71,8 @@ enum : int {
   kBarQEmpty = 3,  // +slot: MMAs of the tile done with the slot
   kBarSFull = 5,   // S^T and dP^T in TMEM
   kBarPFull = 6,   // P^T, dS^T written (4 softmax warps arrive)
-  kBarDqFull = 7,  // dQ tile in TMEM
-  kBarDqEmpty = 8, // dQ tile read (4 drain warps arrive)
-  kBarDone = 9,    // every MMA of the CTA done: dK, dV final
-  kBarDrain = 10,
+  kBarDone = 7,    // every MMA of the CTA done: dK, dV final
+  kBarDrain = 8,
 };
 
 // Query tiles of the lap of K/V block jb, in the order the block visits the ranks.
@@ -114,7 +111,7 @@ __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
 template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1)
-    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
                        const __grid_constant__ BwdArgs a) {
   using L = BSmem<D>;
@@ -148,7 +145,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
       const bool two = i == kBarQFull || i == kBarQFull + 1;
-      const bool four = i == kBarPFull || i == kBarDqEmpty;
+      const bool four = i == kBarPFull;
       mbar_init(bar(i), two ? 2 : (four ? 4 : 1));
     }
     misc[1] = 0;
@@ -222,20 +219,16 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const bool leader = elect_one();
     constexpr uint32_t idesc_s = idesc_bf16_f32(kT, kT, false, false);  // S^T, dP^T: M = keys, N = queries
     constexpr uint32_t idesc_g = idesc_bf16_f32(kT, D, false, true);    // dV, dK: A in TMEM, B MN-major
-    constexpr uint32_t idesc_q = idesc_bf16_f32(kT, D, true, true);     // dQ: A and B MN-major
     const uint64_t k_km = smem_desc_sw128(sb + L::kOffK, 16, 1024);
     const uint64_t v_km = smem_desc_sw128(sb + L::kOffV, 16, 1024);
     const uint64_t q_km = smem_desc_sw128(sb + L::kOffQ, 16, 1024);
     const uint64_t o_km = smem_desc_sw128(sb + L::kOffO, 16, 1024);
     const uint64_t q_mn = smem_desc_sw128(sb + L::kOffQ, L::kHalf, 1024);
     const uint64_t o_mn = smem_desc_sw128(sb + L::kOffO, L::kHalf, 1024);
-    const uint64_t k_mn = smem_desc_sw128(sb + L::kOffK, L::kHalf, 1024);
-    const uint64_t ds_mn = smem_desc_sw128(sb + L::kOffDS, L::kHalf, 1024);
-    const uint32_t km_hi = static_cast<uint32_t>(k_km >> 32), mn_hi = static_cast<uint32_t>(k_mn >> 32);
+    const uint32_t km_hi = static_cast<uint32_t>(k_km >> 32), mn_hi = static_cast<uint32_t>(q_mn >> 32);
     const uint32_t k_km_lo = static_cast<uint32_t>(k_km), v_km_lo = static_cast<uint32_t>(v_km);
     const uint32_t q_km_lo = static_cast<uint32_t>(q_km), o_km_lo = static_cast<uint32_t>(o_km);
     const uint32_t q_mn_lo = static_cast<uint32_t>(q_mn), o_mn_lo = static_cast<uint32_t>(o_mn);
-    const uint32_t k_mn_lo = static_cast<uint32_t>(k_mn), ds_mn_lo = static_cast<uint32_t>(ds_mn);
     auto commit = [&](uint32_t bar_addr) {
       if (leader) mma_commit(bar_addr);
     };
@@ -255,12 +248,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         if (leader) mma_ss_lohi(tmem, k_km_lo + kstep(kk), km_hi, q_km_lo + slot + kstep(kk), km_hi, idesc_s, kk > 0);
-      // 2. dP^T = V dO^T, once the previous dQ tile has left its columns
-      if (it > 0 && !mbar_wait_bounded(bar(kBarDqEmpty), (it - 1) & 1, abort_flag, a.err, tmo)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      // 2. dP^T = V dO^T
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         if (leader)
@@ -280,12 +268,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       for (int kk = 0; kk < kT / 16; ++kk)
         if (leader) mma_ts_lohi(tmem + 256 + D, tmem + 128 + kk * 8, q_mn_lo + slot + ((kk * 2048) >> 4), mn_hi,
                                 idesc_g, (it > 0 || kk > 0) ? 1u : 0u);
-      // 5. dQ = dS K   (K = keys: 16 key rows = 2048 bytes of both MN-major tiles)
-#pragma unroll
-      for (int kk = 0; kk < kT / 16; ++kk)
-        if (leader) mma_ss_lohi(tmem + 128, ds_mn_lo + ((kk * 2048) >> 4), mn_hi, k_mn_lo + ((kk * 2048) >> 4), mn_hi,
-                                idesc_q, kk > 0);
-      commit(bar(kBarDqFull));
       commit(bar(kBarQEmpty + s));
     }
     if (ok) {
@@ -294,7 +276,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       commit(bar(kBarDrain));
       drain_wait_b(bar(kBarDrain), 0, tmo);
     }
-  } else if (warp < 6) {
+  } else {
     // ===================== softmax: one thread per key row =====================
     const int wq = warp & 3;
     const int key = wq * 32 + lane;
@@ -302,7 +284,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
     const bool kvalid = key < nk;
     const float c2 = a.scale * kLog2eB;
-    uint8_t* ds_row = smem + L::kOffDS + key * 128;
     bool ok = true;
     for (int it = 0; it < NQT; ++it) {
       const int s = it & 1;
@@ -348,17 +329,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         // P^T over S^T's consumed columns, dS^T over dP^T's consumed columns
         tmem_st16(t_s + c * 16, pp);
         tmem_st16(t_dp + c * 16, dd);
-        // dS^T row `key`, queries c*32 .. c*32+31: box c/2, 16-byte units (c%2)*4 .. +3, 128-byte swizzle
-        uint8_t* box = ds_row + (c >> 1) * L::kHalf;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int unit = (c & 1) * 4 + u;
-          *reinterpret_cast<uint4*>(box + ((unit ^ (key & 7)) << 4)) =
-              make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
-        }
       }
       tmem_wait_st();
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarPFull));
@@ -386,34 +358,293 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         }
       }
     }
+  }
+
+  // ---- teardown: every thread of the CTA arrives here, aborted or not ----
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemColsB);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// dq: one CTA per 128 query rows of one (batch entry, head); Q and dO loaded
+// once, K and V tiles of the rank's lap streamed in ring order ((r - t) mod n)
+// through two stages. Per K/V tile three MMAs (M = 128 query rows):
+//   S  = Q K^T    (SS, both K-major)                     -> TMEM [0, 128)
+//   dP = dO V^T   (SS)                                   -> TMEM [128, 256)
+//   dQ += dS K    (TS: dS in TMEM over S's consumed columns, K read MN-major)
+//                                                        -> TMEM [256, 256 + D)
+// Warps 2-5 (one thread per query row, lse and delta in registers) form
+// dS = p (dp - delta) between the first two and the third. dq is stored once,
+// without atomics.
+// ----------------------------------------------------------------------------
+template <int D>
+struct DqSmem {
+  static constexpr int kTile = kT * D * 2;
+  static constexpr int kHalf = kT * 128;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffO = kTile;
+  static constexpr int kOffK = 2 * kTile;  // two stages
+  static constexpr int kOffV = 4 * kTile;  // two stages
+  static constexpr int kOffBar = 6 * kTile;
+  static constexpr int kNumBars = 9;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kMax = 227 * 1024;
+  static constexpr int kAlloc = kBytes + 1024 <= kMax ? kBytes + 1024 : kMax;
+};
+
+enum : int {
+  kDqBarQ = 0,        // Q and dO landed
+  kDqBarKVFull = 1,   // +stage: K and V tiles landed
+  kDqBarKVEmpty = 3,  // +stage: MMAs done with the stage
+  kDqBarSFull = 5,    // S and dP in TMEM
+  kDqBarPFull = 6,    // dS written (4 softmax warps arrive)
+  kDqBarDone = 7,     // every MMA done: dQ final
+  kDqBarDrain = 8,
+};
+
+// K/V tiles of rank r's lap, blocks in ring order (r - t) mod n.
+struct KvWalk {
+  int t, tile, ntile, off, len;
+  __device__ __forceinline__ void init(const BwdArgs& a, int r) {
+    t = -1;
+    next_block(a, r);
+  }
+  __device__ __forceinline__ void next_block(const BwdArgs& a, int r) {
+    tile = 0;
+    while (true) {
+      ++t;
+      if (t >= a.n) return;
+      int j = (r - t) % a.n;
+      if (j < 0) j += a.n;
+      off = a.off[j];
+      len = a.len[j];
+      ntile = (len + kT - 1) / kT;
+      if (ntile > 0) return;
+    }
+  }
+  __device__ __forceinline__ int k0() const { return off + tile * kT; }
+  __device__ __forceinline__ int nvalid() const { return min(kT, len - tile * kT); }
+  __device__ __forceinline__ void advance(const BwdArgs& a, int r) {
+    if (++tile >= ntile) next_block(a, r);
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                          const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                          const __grid_constant__ BwdArgs a) {
+  using L = DqSmem<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+  if (pad > static_cast<uint32_t>(L::kAlloc - L::kBytes)) {
+    if (threadIdx.x == 0) atomicOr(a.err, kDevErrLayout);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = smem_addr(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);  // [0] TMEM base, [1] abort flag
+  volatile uint32_t* abort_flag = misc + 1;
+  auto bar = [&](int i) -> uint32_t { return sb + L::kOffBar + 8 * i; };
+
+  const int h = blockIdx.y, b = blockIdx.z;
+  int r = 0;
+  while (r + 1 < a.n && a.q_prefix[r + 1] <= static_cast<int>(blockIdx.x)) ++r;
+  const int q0 = a.off[r] + (static_cast<int>(blockIdx.x) - a.q_prefix[r]) * kT;
+  const int nq = min(kT, a.off[r] + a.len[r] - q0);
+  int NT = 0;
+  for (int t = 0; t < a.n; ++t) {
+    int j = (r - t) % a.n;
+    if (j < 0) j += a.n;
+    NT += (a.len[j] + kT - 1) / kT;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), i == kDqBarPFull ? 4 : 1);
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(misc), kTmemColsB);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const uint64_t tmo = a.timeout_ns;
+
+  if (warp == 0) {
+    // ===================== TMA producer =====================
+    const bool leader = elect_one();
+    if (leader) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&to);
+      mbar_arrive_expect_tx(bar(kDqBarQ), 2 * L::kTile);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_4d(sb + L::kOffQ + c * L::kHalf, &tq, bar(kDqBarQ), c * 64, h, q0, b);
+        tma_load_4d(sb + L::kOffO + c * L::kHalf, &to, bar(kDqBarQ), c * 64, h, q0, b);
+      }
+    }
+    int issued[2] = {0, 0};
+    KvWalk cur;
+    cur.init(a, r);
+    for (int it = 0; it < NT; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kDqBarKVEmpty + s), ph ^ 1, abort_flag, a.err, tmo)))
+        break;
+      if (leader) {
+        mbar_arrive_expect_tx(bar(kDqBarKVFull + s), 2 * L::kTile);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(sb + L::kOffK + s * L::kTile + c * L::kHalf, &tk, bar(kDqBarKVFull + s), c * 64, h, cur.k0(),
+                      b);
+          tma_load_4d(sb + L::kOffV + s * L::kTile + c * L::kHalf, &tv, bar(kDqBarKVFull + s), c * 64, h, cur.k0(),
+                      b);
+        }
+      }
+      ++issued[s];
+      cur.advance(a, r);
+    }
+    if (*abort_flag) {
+      // let every issued copy land before the CTA's shared memory goes away
+      drain_wait_b(bar(kDqBarQ), 0, tmo);
+      for (int s = 0; s < 2; ++s)
+        if (issued[s]) drain_wait_b(bar(kDqBarKVFull + s), (issued[s] - 1) & 1, tmo);
+    }
+  } else if (warp == 1) {
+    // ===================== MMA issuer =====================
+    const bool leader = elect_one();
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kT, kT, false, false);  // S, dP: M = query rows, N = keys
+    constexpr uint32_t idesc_q = idesc_bf16_f32(kT, D, false, true);    // dQ: A (dS) in TMEM, B (K) MN-major
+    const uint64_t q_km = smem_desc_sw128(sb + L::kOffQ, 16, 1024);
+    const uint64_t o_km = smem_desc_sw128(sb + L::kOffO, 16, 1024);
+    const uint64_t k_km = smem_desc_sw128(sb + L::kOffK, 16, 1024);
+    const uint64_t v_km = smem_desc_sw128(sb + L::kOffV, 16, 1024);
+    const uint64_t k_mn = smem_desc_sw128(sb + L::kOffK, L::kHalf, 1024);
+    const uint32_t km_hi = static_cast<uint32_t>(q_km >> 32), mn_hi = static_cast<uint32_t>(k_mn >> 32);
+    const uint32_t q_lo = static_cast<uint32_t>(q_km), o_lo = static_cast<uint32_t>(o_km);
+    const uint32_t k_lo = static_cast<uint32_t>(k_km), v_lo = static_cast<uint32_t>(v_km);
+    const uint32_t k_mn_lo = static_cast<uint32_t>(k_mn);
+    auto commit = [&](uint32_t bar_addr) {
+      if (leader) mma_commit(bar_addr);
+    };
+    auto kstep = [](int kk) -> uint32_t { return static_cast<uint32_t>(((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4); };
+    bool ok = mbar_wait_bounded(bar(kDqBarQ), 0, abort_flag, a.err, tmo);
+    for (int it = 0; ok && it < NT; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      const uint32_t stage = static_cast<uint32_t>((s * L::kTile) >> 4);
+      if (!mbar_wait_bounded(bar(kDqBarKVFull + s), ph, abort_flag, a.err, tmo)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        if (leader) mma_ss_lohi(tmem, q_lo + kstep(kk), km_hi, k_lo + stage + kstep(kk), km_hi, idesc_s, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        if (leader) mma_ss_lohi(tmem + 128, o_lo + kstep(kk), km_hi, v_lo + stage + kstep(kk), km_hi, idesc_s, kk > 0);
+      commit(bar(kDqBarSFull));
+      if (!mbar_wait_bounded(bar(kDqBarPFull), it & 1, abort_flag, a.err, tmo)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // dQ += dS K   (K = keys: 16 key rows = 2048 bytes of the MN-major K tile)
+#pragma unroll
+      for (int kk = 0; kk < kT / 16; ++kk)
+        if (leader) mma_ts_lohi(tmem + 256, tmem + kk * 8, k_mn_lo + stage + ((kk * 2048) >> 4), mn_hi, idesc_q,
+                                (it > 0 || kk > 0) ? 1u : 0u);
+      commit(bar(kDqBarKVEmpty + s));
+    }
+    if (ok) {
+      commit(bar(kDqBarDone));
+    } else {
+      commit(bar(kDqBarDrain));
+      drain_wait_b(bar(kDqBarDrain), 0, tmo);
+    }
   } else {
-    // ===================== dQ drain: one thread per query row =====================
+    // ===================== dS: one thread per query row =====================
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
-    const uint32_t t_q = tmem + (static_cast<uint32_t>(wq * 32) << 16) + 128;
-    QCursor cur;
-    cur.init(a, jb);
-    for (int it = 0; it < NQT; ++it) {
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarDqFull), it & 1, abort_flag, a.err, tmo))) break;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
+    const float c2 = a.scale * kLog2eB;
+    // the row's lse (times log2 e) and delta; a row past the shard, or one that
+    // saw no key, gets lse = +inf so that p = 0
+    float nl2 = -INFINITY, ndl = 0.f;
+    if (row < nq) {
+      const int64_t o = b * a.l_bstride + static_cast<int64_t>(h) * a.S + q0 + row;
+      const float l = a.lse[o];
+      nl2 = l == -INFINITY ? -INFINITY : -l * kLog2eB;
+      ndl = -a.delta[o];
+    }
+    bool ok = true;
+    KvWalk cur;
+    cur.init(a, r);
+    for (int it = 0; it < NT; ++it) {
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kDqBarSFull), it & 1, abort_flag, a.err, tmo));
+      if (!ok) break;
       tc_fence_after();
-      uint32_t r[D / 32][32];
+      const int nvk = cur.nvalid();
+#pragma unroll 1
+      for (int c = 0; c < kT / 32; ++c) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(t_s + c * 32, sr);
+        tmem_ld32(t_dp + c * 32, dr);
+        tmem_wait_ld();
+        uint32_t dd[16];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(t_q + c * 32, r[c]);
-      tmem_wait_ld();
+        for (int e = 0; e < 32; e += 2) {
+          float t0, t1, g0, g1, d0, d1;
+          fma_f32x2(t0, t1, u2f(sr[e]), u2f(sr[e + 1]), c2, nl2);
+          fma_f32x2(g0, g1, u2f(dr[e]), u2f(dr[e + 1]), 1.f, ndl);
+          const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+          fma2(d0, d1, p0, p1, g0, g1, 0.f, 0.f);
+          // keys past the K/V tile (the next block's rows, or zero fill) take no part
+          d0 = c * 32 + e < nvk ? d0 : 0.f;
+          d1 = c * 32 + e + 1 < nvk ? d1 : 0.f;
+          dd[e >> 1] = pack_bf16x2(d0, d1);
+        }
+        // dS over S's consumed columns
+        tmem_st16(t_s + c * 16, dd);
+      }
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarDqEmpty));
-      if (row < cur.nvalid()) {
-        float* dst = a.dq + b * a.bstride + static_cast<int64_t>(cur.q0() + row) * a.sstride + h * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c)
+      if (lane == 0) mbar_arrive(bar(kDqBarPFull));
+      cur.advance(a, r);
+    }
+    // ---- dq of this CTA's rows ----
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kDqBarDone), 0, abort_flag, a.err, tmo));
+    if (ok) {
+      tc_fence_after();
+      float* dst = a.dq + b * a.bstride + static_cast<int64_t>(q0 + row) * a.sstride + h * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_off + 256 + c * 32, rr);
+        tmem_wait_ld();
+        if (row < nq) {
 #pragma unroll
           for (int x = 0; x < 32; x += 4)
-            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + x),
-                      make_float4(u2f(r[c][x]) * a.scale, u2f(r[c][x + 1]) * a.scale, u2f(r[c][x + 2]) * a.scale,
-                                  u2f(r[c][x + 3]) * a.scale));
+            *reinterpret_cast<float4*>(dst + c * 32 + x) =
+                make_float4(u2f(rr[x]) * a.scale, u2f(rr[x + 1]) * a.scale, u2f(rr[x + 2]) * a.scale,
+                            u2f(rr[x + 3]) * a.scale);
+        }
       }
-      cur.advance(a, jb);
     }
   }
 
@@ -431,13 +662,23 @@ template <int D>
 cudaError_t launch_bwd_tc_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& to, cudaStream_t s) {
   using L = BSmem<D>;
-  static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  using LQ = DqSmem<D>;
+  static_assert(L::kAlloc <= 227 * 1024 && LQ::kAlloc <= 227 * 1024, "shared memory budget");
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  const int tiles = a.kv_prefix[a.n];
-  if (tiles == 0 || a.H == 0 || a.B == 0) return cudaSuccess;
-  attn_bwd_tc_kernel<D><<<dim3(tiles, a.H, a.B), kThreadsB, L::kAlloc, s>>>(tq, tk, tv, to, a);
-  return cudaGetLastError();
+  e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LQ::kAlloc);
+  if (e != cudaSuccess) return e;
+  if (a.H == 0 || a.B == 0) return cudaSuccess;
+  if (a.kv_prefix[a.n] > 0) {
+    attn_bwd_dkdv_tc_kernel<D><<<dim3(a.kv_prefix[a.n], a.H, a.B), kThreadsB, L::kAlloc, s>>>(tq, tk, tv, to, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (a.q_prefix[a.n] > 0) {
+    attn_bwd_dq_tc_kernel<D><<<dim3(a.q_prefix[a.n], a.H, a.B), kThreadsB, LQ::kAlloc, s>>>(tq, tk, tv, to, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace

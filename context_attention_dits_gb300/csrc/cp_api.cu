@@ -924,7 +924,7 @@ size_t cp_attention_bwd_workspace_size(int B, int H, int S, int D, int ring_degr
 int cp_attention_bwd_launch_count(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt) {
   if (B <= 0 || S <= 0 || H < 1 || D < 1 || ring_degree < 1 || ulysses_degree < 1) return 0;
   const int U = ulysses_degree;
-  int n = dt == CP_BF16 ? 2 : 3;  // delta, then the tensor-core kernel, or the dq and dk/dv kernels
+  int n = 3;  // delta, then the dk/dv and dq kernels (tensor cores for bf16, CUDA cores for fp32)
   if (U > 1 && H % U == 0) {
     const BwdWs w = bwd_ws_layout(B, H, S, D, U, dt);
     char* base = reinterpret_cast<char*>(uintptr_t{1} << 20);
@@ -967,10 +967,7 @@ cp_status cp_attention_bwd(const void* q, const void* k, const void* v, const fl
   char* ws = static_cast<char*>(workspace);
   const bool bf16 = dt == CP_BF16;
   float* delta = reinterpret_cast<float*>(ws + w.delta);
-  // the tensor-core kernel accumulates dq with atomics: the delta launch zeroes it
-  float* dq_acc = U > 1 ? reinterpret_cast<float*>(ws + w.dqh) : dq;
-  if (cp::launch_attn_bwd_delta(out, dout, delta, bf16 ? dq_acc : nullptr, B, S, H, D, bf16, s) != cudaSuccess)
-    return CP_ERR_CUDA;
+  if (cp::launch_attn_bwd_delta(out, dout, delta, nullptr, B, S, H, D, bf16, s) != cudaSuccess) return CP_ERR_CUDA;
 
   cp::BwdArgs a{};
   a.n = R;
