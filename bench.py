@@ -287,7 +287,7 @@ def secondary(cpa, dev, flush, stream, peaks):
         tf = 2.5 * w.flops / (ms * 1e-3) / 1e12
         res[name] = {"TFLOP_s": tf, "ms": ms, "frac_of_bf16_peak": tf / bf16,
                      "launches": cpa.cp_attention_bwd_launch_count(w.B, w.H, w.S, w.D, R, U, q.dtype),
-                     "note": "tensor-core backward, dq by fp32 atomics; FLOPs = 2.5 x forward"}
+                     "note": "tensor-core backward (dk/dv and dq kernels); FLOPs = 2.5 x forward"}
         del q, k, v, dout, out, lse, grads, ws
     if cpa.cp_check_device_status() != 0:
         raise RuntimeError("device status after the secondary measurements")

@@ -113,8 +113,7 @@ __device__ __forceinline__ int shard_of(const int* prefix, int n, int item) {
 template <int D, typename T>
 __global__ void __launch_bounds__(kBwdThreads) attn_bwd_delta_kernel(const float* __restrict__ out,
                                                                      const T* __restrict__ dout,
-                                                                     float* __restrict__ delta,
-                                                                     float* __restrict__ zero, int B, int S, int H) {
+                                                                     float* __restrict__ delta, int B, int S, int H) {
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (kBwdThreads / 32) + (threadIdx.x >> 5);
   if (row >= static_cast<int64_t>(B) * S * H) return;
@@ -130,9 +129,6 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_delta_kernel(const float
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) delta[(b * H + h) * S + s] = acc;
-  if (zero != nullptr)
-    for (int d = lane * 4; d < D; d += 128)
-      *reinterpret_cast<float4*>(zero + row * D + d) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ----------------------------------------------------------------------------
@@ -399,12 +395,11 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t s) {
 }
 
 template <int D, typename T>
-cudaError_t launch_delta_d(const float* out, const void* dout, float* delta, float* zero, int B, int S, int H,
-                           cudaStream_t s) {
+cudaError_t launch_delta_d(const float* out, const void* dout, float* delta, int B, int S, int H, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(B) * S * H;
   const int64_t blocks = (rows + kBwdThreads / 32 - 1) / (kBwdThreads / 32);
   attn_bwd_delta_kernel<D, T><<<static_cast<unsigned>(blocks), kBwdThreads, 0, s>>>(
-      out, static_cast<const T*>(dout), delta, zero, B, S, H);
+      out, static_cast<const T*>(dout), delta, B, S, H);
   return cudaGetLastError();
 }
 
@@ -416,15 +411,15 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, int D, bool bf16, cudaStream_t s) 
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attn_bwd_delta(const float* out, const void* dout, float* delta, float* zero, int B, int S, int H,
-                                  int D, bool bf16, cudaStream_t s) {
+cudaError_t launch_attn_bwd_delta(const float* out, const void* dout, float* delta, int B, int S, int H, int D,
+                                  bool bf16, cudaStream_t s) {
   if (static_cast<int64_t>(B) * S * H == 0) return cudaSuccess;
   if (D == 128)
-    return bf16 ? launch_delta_d<128, __nv_bfloat16>(out, dout, delta, zero, B, S, H, s)
-                : launch_delta_d<128, float>(out, dout, delta, zero, B, S, H, s);
+    return bf16 ? launch_delta_d<128, __nv_bfloat16>(out, dout, delta, B, S, H, s)
+                : launch_delta_d<128, float>(out, dout, delta, B, S, H, s);
   if (D == 64)
-    return bf16 ? launch_delta_d<64, __nv_bfloat16>(out, dout, delta, zero, B, S, H, s)
-                : launch_delta_d<64, float>(out, dout, delta, zero, B, S, H, s);
+    return bf16 ? launch_delta_d<64, __nv_bfloat16>(out, dout, delta, B, S, H, s)
+                : launch_delta_d<64, float>(out, dout, delta, B, S, H, s);
   return cudaErrorInvalidValue;
 }
 

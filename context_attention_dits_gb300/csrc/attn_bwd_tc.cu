@@ -6,26 +6,27 @@
 //   p_ij = exp(scale q_i.k_j - lse_i),  ds_ij = p_ij (dout_i.v_j - delta_i),
 //   dv_j = sum_i p_ij dout_i,  dk_j = scale sum_i ds_ij q_i,  dq_i = scale sum_j ds_ij k_j.
 //
-// One CTA owns a tile of 128 keys of one (batch entry, head) and walks every
-// 128-row query tile of the lap, rank by rank in the order its K/V block
-// visits them ((j + t) mod n). Per query tile, five MMAs (M = 128):
-//   1. S^T  = K Q^T           (A = K tile, B = Q tile; both K-major)  -> TMEM [0, 128)
-//   2. dP^T = V dO^T          (A = V tile, B = dO tile)               -> TMEM [128, 256)
-//   3. dV  += P^T dO          (A = P^T in TMEM, B = dO MN-major)      -> TMEM [256, 256 + D)
-//   4. dK  += dS^T Q          (A = dS^T in TMEM, B = Q MN-major)      -> TMEM [256 + D, 256 + 2D)
-//   5. dQ   = dS K            (A = dS^T in shared memory read MN-major,
-//                              B = K tile MN-major)                   -> TMEM [128, 128 + D)
+// Two kernels, neither with atomics:
+//
+// dk / dv: one CTA owns a tile of 128 keys of one (batch entry, head) and
+// walks every 128-row query tile of the lap, rank by rank in the order its
+// K/V block visits them ((j + t) mod n). Per query tile, four MMAs (M = 128):
+//   1. S^T  = K Q^T      (A = K tile, B = Q tile; both K-major)  -> TMEM [0, 128)
+//   2. dP^T = V dO^T     (A = V tile, B = dO tile)               -> TMEM [128, 256)
+//   3. dV  += P^T dO     (A = P^T in TMEM, B = dO MN-major)      -> TMEM [256, 256 + D)
+//   4. dK  += dS^T Q     (A = dS^T in TMEM, B = Q MN-major)      -> TMEM [256 + D, 256 + 2D)
 // Between 2 and 3 the softmax warpgroup (one thread per key row) turns S^T
 // and dP^T into P^T (bf16, over S^T's first 64 columns) and dS^T (bf16, over
-// dP^T's first 64 columns, and into shared memory in the 128-byte-swizzled
-// layout that MMA 5 reads). A second warpgroup (one thread per query row)
-// drains each dQ tile and adds it into the fp32 dq in global memory with
-// 16-byte atomics; dq must start at zero. After the last query tile the
-// softmax warpgroup writes dk and dv once.
+// dP^T's first 64 columns). After the last query tile it writes dk and dv.
 //
-// Warp roles (320 threads): 0 = TMA producer (K, V once; Q, dO and the rows'
-// lse and delta per query tile, double-buffered), 1 = MMA issuer, 2-5 =
-// softmax, 6-9 = dQ drain. A warp reaches TMEM lanes 32 (warp mod 4) and up.
+// dq: one CTA owns 128 query rows and walks the K/V tiles of its rank's lap
+// in ring order ((r - t) mod n): S = Q K^T, dP = dO V^T, then dQ += dS K with
+// dS (a thread per query row) in TMEM over S's consumed columns; dq is
+// stored once. It recomputes S and dP, 1.4x the MMA work of a single fused
+// kernel, in exchange for no reduction of dq tiles across key-tile CTAs.
+//
+// Warp roles (192 threads): 0 = TMA producer, 1 = MMA issuer, 2-5 = the
+// thread-per-row warpgroup (a warp reaches TMEM lanes 32 (warp mod 4) and up).
 // Every wait is bounded; on expiry the CTA records a timeout, lets its copies
 // land, frees its tensor memory and returns.
 #include <cuda.h>
@@ -116,9 +117,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                        const __grid_constant__ BwdArgs a) {
   using L = BSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // the swizzled tiles need a 1024-byte aligned base; with D = 128 the budget
-  // leaves less than 1024 bytes of slack, so a base that would need more is
-  // reported (uniformly, before any barrier or TMEM use) instead of used
+  // the swizzled tiles need a 1024-byte aligned base; a base that would need
+  // more padding than the allocation holds is reported (uniformly, before any
+  // barrier or TMEM use) instead of used
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
   if (pad > static_cast<uint32_t>(L::kAlloc - L::kBytes)) {
     if (threadIdx.x == 0) atomicOr(a.err, kDevErrLayout);

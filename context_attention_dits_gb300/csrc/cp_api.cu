@@ -967,7 +967,7 @@ cp_status cp_attention_bwd(const void* q, const void* k, const void* v, const fl
   char* ws = static_cast<char*>(workspace);
   const bool bf16 = dt == CP_BF16;
   float* delta = reinterpret_cast<float*>(ws + w.delta);
-  if (cp::launch_attn_bwd_delta(out, dout, delta, nullptr, B, S, H, D, bf16, s) != cudaSuccess) return CP_ERR_CUDA;
+  if (cp::launch_attn_bwd_delta(out, dout, delta, B, S, H, D, bf16, s) != cudaSuccess) return CP_ERR_CUDA;
 
   cp::BwdArgs a{};
   a.n = R;
@@ -983,7 +983,7 @@ cp_status cp_attention_bwd(const void* q, const void* k, const void* v, const fl
   a.scale = scale;
   a.err = dev->err;
   a.timeout_ns = kWaitTimeoutNs;
-  // bf16: tensor maps over the (possibly head-grouped) q, k, v, dout, then the tensor-core kernel
+  // bf16: tensor maps over the (possibly head-grouped) q, k, v, dout, then the tensor-core kernels
   auto run = [&](int Bn, int Hx) -> cp_status {
     if (!bf16) return cp::launch_attn_bwd(a, D, false, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
     CUtensorMap tq, tk, tv, to;

@@ -102,21 +102,21 @@ struct BwdArgs {
   float* dq;
   float* dk;
   float* dv;
-  // tensor-core kernel: device error word and the bound on each device-side wait
+  // tensor-core kernels: device error word and the bound on each device-side wait
   uint32_t* err;
   uint64_t timeout_ns;
 };
-constexpr int kBwdTcTile = 128;  // keys per tensor-core backward CTA, query rows per step
+constexpr int kBwdTcTile = 128;  // tensor-core backward: keys or query rows per CTA and per step
 
 // Launchers (each returns the launch error, cudaSuccess if none).
 // dq, then dk/dv, for D in {64, 128}; bf16 or fp32 inputs.
 cudaError_t launch_attn_bwd(const BwdArgs& a, int D, bool bf16, cudaStream_t s);
-// delta[b, h, s] = sum_d out[b, s, h, d] * dout[b, s, h, d] over dense [B, S, H, D];
-// when zero != nullptr also zero[0 .. B*S*H*D) = 0 (the tensor-core backward's dq accumulator).
-cudaError_t launch_attn_bwd_delta(const float* out, const void* dout, float* delta, float* zero, int B, int S, int H,
-                                  int D, bool bf16, cudaStream_t s);
+// delta[b, h, s] = sum_d out[b, s, h, d] * dout[b, s, h, d] over dense [B, S, H, D].
+cudaError_t launch_attn_bwd_delta(const float* out, const void* dout, float* delta, int B, int S, int H, int D,
+                                  bool bf16, cudaStream_t s);
 // Tensor-core backward for bf16 q, k, v, dout with tensor maps of box {64, 1, 128, 1}
-// (128-byte swizzle): dk, dv written, dq accumulated (it must hold zeros).
+// (128-byte swizzle): the dk/dv kernel (one CTA per 128 keys, kv_prefix) and the
+// dq kernel (one CTA per 128 query rows, q_prefix); dq, dk, dv written.
 cudaError_t launch_attn_bwd_tc(const BwdArgs& a, int D, const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,

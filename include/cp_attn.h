@@ -345,9 +345,9 @@ int cp_attention_bwd_launch_count(int B, int H, int S, int D, int ring_degree, i
  *   workspace     : device, >= cp_attention_bwd_workspace_size(...) bytes,
  *                   256-byte aligned, owned by the caller.
  * bf16 runs on the tensor cores: bf16 operands (P and dS rounded to bf16
- * for their products), fp32 accumulation, dq accumulated with fp32 atomics
- * (its summation order varies from run to run). fp32 runs on the CUDA cores
- * in fp32 throughout. Asynchronous on `stream`.
+ * for their products), fp32 accumulation. fp32 runs on the CUDA cores in
+ * fp32 throughout. Results are deterministic (no atomics). Asynchronous on
+ * `stream`.
  * Errors (returned before any launch): the checks of cp_attention_validate
  * with uneven_ok = 0; uneven_ok != 0 -> CP_ERR_UNSUPPORTED_COMBO (the
  * Anything variants have no backward); a null pointer or non-finite scale ->
