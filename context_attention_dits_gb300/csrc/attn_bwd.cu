@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
   const T* v = static_cast<const T*>(a.v);
   const T* dout = static_cast<const T*>(a.dout);
   const int tid = threadIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (bwd_head_is_padding(a, h, b)) return;
   const int r = shard_of(a.q_prefix, a.n, blockIdx.x);
   const int row0 = a.off[r] + (blockIdx.x - a.q_prefix[r]) * kBT;
   const int nrows = min(kBT, a.off[r] + a.len[r] - row0);
@@ -273,6 +274,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
   const T* v = static_cast<const T*>(a.v);
   const T* dout = static_cast<const T*>(a.dout);
   const int tid = threadIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (bwd_head_is_padding(a, h, b)) return;
   const int jb = shard_of(a.kv_prefix, a.n, blockIdx.x);
   const int key0 = a.off[jb] + (blockIdx.x - a.kv_prefix[jb]) * kBT;
   const int nk = min(kBT, a.off[jb] + a.len[jb] - key0);

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   float* s_dlt = reinterpret_cast<float*>(smem + L::kOffDlt);
 
   const int h = blockIdx.y, b = blockIdx.z;
+  if (bwd_head_is_padding(a, h, b)) return;  // uniform per CTA, before any barrier or TMEM
   int jb = 0;
   while (jb + 1 < a.n && a.kv_prefix[jb + 1] <= static_cast<int>(blockIdx.x)) ++jb;
   const int key0 = a.off[jb] + (static_cast<int>(blockIdx.x) - a.kv_prefix[jb]) * kT;
@@ -457,6 +458,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   auto bar = [&](int i) -> uint32_t { return sb + L::kOffBar + 8 * i; };
 
   const int h = blockIdx.y, b = blockIdx.z;
+  if (bwd_head_is_padding(a, h, b)) return;  // uniform per CTA, before any barrier or TMEM
   int r = 0;
   while (r + 1 < a.n && a.q_prefix[r + 1] <= static_cast<int>(blockIdx.x)) ++r;
   const int q0 = a.off[r] + (static_cast<int>(blockIdx.x) - a.q_prefix[r]) * kT;

@@ -858,14 +858,16 @@ struct BwdWs {
 
 BwdWs bwd_ws_layout(int B, int H, int S, int D, int U, cp_dtype dt) {
   BwdWs w;
-  const size_t n = static_cast<size_t>(B) * S * H * D, nl = static_cast<size_t>(B) * H * S;
+  // U head groups of ceil(H/U) heads (the last head of a short group is padding)
+  const size_t Hp = U > 1 ? static_cast<size_t>((H + U - 1) / U) * U : static_cast<size_t>(H);
+  const size_t n = static_cast<size_t>(B) * S * Hp * D, nl = static_cast<size_t>(B) * Hp * S;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
     o = round_up(o + bytes, 256);
     return at;
   };
-  w.delta = take(nl * 4);
+  w.delta = take(static_cast<size_t>(B) * H * S * 4);
   if (U > 1) {
     w.qh = take(n * elem_size(dt));
     w.kh = take(n * elem_size(dt));
@@ -882,34 +884,67 @@ BwdWs bwd_ws_layout(int B, int H, int S, int D, int U, cp_dtype dt) {
 }
 
 cp_status bwd_validate(int B, int H, int S, int D, int R, int U, int uneven_ok, cp_dtype dt) {
-  // the Anything variants have no backward: Ring Anything is inference only
-  if (uneven_ok) return CP_ERR_UNSUPPORTED_COMBO;
-  return cp_attention_validate(B, H, S, D, R, U, 0, dt);
+  // Ring Anything is inference only; Ulysses Anything has a backward
+  if (uneven_ok && R > 1) return CP_ERR_UNSUPPORTED_COMBO;
+  return cp_attention_validate(B, H, S, D, R, U, uneven_ok, dt);
 }
 
-// Copies of the backward's Ulysses regroups: q, k, v, dout [B,S,H,D] -> [U][B,S,H/U,D]
-// and lse, delta [B,H,S] -> [U][B,H/U,S] (in), or dq, dk, dv back (out).
+// Copies of the backward's Ulysses regroups: q, k, v, dout [B,S,H,D] -> [U][B,S,Hg,D]
+// and lse, delta [B,H,S] -> [U][B,Hg,S] (in), or dq, dk, dv back (out), with
+// Hg = ceil(H/U). With H % U != 0 the head groups are the balanced split and
+// a short group's last head slot is left unwritten (padding).
 void bwd_in_copies(const void* const src[4], void* const dst[4], const float* lse, const float* delta, float* lh,
                    float* dlh, int B, int H, int S, int D, int U, int eb, std::vector<SegCopy>* cs) {
-  const int Hg = H / U;
+  const int Hg = (H + U - 1) / U;
   const int64_t row = static_cast<int64_t>(Hg) * D;
-  for (int i = 0; i < 4; ++i)
-    cs->push_back(SegCopy{src[i], dst[i], 1, U, B, S, 0, row, static_cast<int64_t>(S) * H * D,
-                          static_cast<int64_t>(H) * D, row, eb});
-  // out segments (g, b, h) of S floats <- in[b, g*Hg + h, :]
+  const int64_t grp = static_cast<int64_t>(B) * S * row;  // elements per head group
   const float* ls[2] = {lse, delta};
   float* ld[2] = {lh, dlh};
+  if (H % U == 0) {
+    for (int i = 0; i < 4; ++i)
+      cs->push_back(SegCopy{src[i], dst[i], 1, U, B, S, 0, row, static_cast<int64_t>(S) * H * D,
+                            static_cast<int64_t>(H) * D, row, eb});
+    // out segments (g, b, h) of S floats <- in[b, g*Hg + h, :]
+    for (int i = 0; i < 2; ++i)
+      cs->push_back(SegCopy{ls[i], ld[i], 1, U, B, Hg, 0, static_cast<int64_t>(Hg) * S,
+                            static_cast<int64_t>(H) * S, S, S, 4});
+    return;
+  }
+  std::vector<int> hoff(U), hlen(U);
+  (void)shard_table(H, U, true, hoff.data(), hlen.data());
+  for (int i = 0; i < 4; ++i)
+    for (int g = 0; g < U; ++g)
+      // group g, rows (b, t) of hlen[g]*D elements <- in[b, t, hoff[g] : hoff[g] + hlen[g], :]
+      cs->push_back(SegCopy{static_cast<const char*>(src[i]) + static_cast<int64_t>(hoff[g]) * D * eb,
+                            static_cast<char*>(dst[i]) + g * grp * eb, 1, 1, B, S, 0, 0,
+                            static_cast<int64_t>(S) * H * D, static_cast<int64_t>(H) * D,
+                            static_cast<int64_t>(hlen[g]) * D, eb, 0, 0, S * row, row});
   for (int i = 0; i < 2; ++i)
-    cs->push_back(SegCopy{ls[i], ld[i], 1, U, B, Hg, 0, static_cast<int64_t>(Hg) * S, static_cast<int64_t>(H) * S,
-                          S, S, 4});
+    for (int g = 0; g < U; ++g)
+      // group g's [b, h, :] <- in[b, hoff[g] + h, :], h < hlen[g]
+      cs->push_back(SegCopy{ls[i] + static_cast<int64_t>(hoff[g]) * S, ld[i] + static_cast<int64_t>(g) * B * Hg * S,
+                            1, 1, B, hlen[g], 0, 0, static_cast<int64_t>(H) * S, S, S, 4, 0, 0,
+                            static_cast<int64_t>(Hg) * S, S});
 }
 
 void bwd_out_copies(const float* const src[3], float* const dst[3], int B, int H, int S, int D, int U,
                     std::vector<SegCopy>* cs) {
-  const int Hg = H / U;
+  const int Hg = (H + U - 1) / U;
   const int64_t row = static_cast<int64_t>(Hg) * D, bstride = S * row;
+  if (H % U == 0) {
+    for (int i = 0; i < 3; ++i)
+      cs->push_back(
+          SegCopy{src[i], dst[i], 1, B, S, U, 0, bstride, row, static_cast<int64_t>(B) * bstride, row, 4});
+    return;
+  }
+  std::vector<int> hoff(U), hlen(U);
+  (void)shard_table(H, U, true, hoff.data(), hlen.data());
   for (int i = 0; i < 3; ++i)
-    cs->push_back(SegCopy{src[i], dst[i], 1, B, S, U, 0, bstride, row, static_cast<int64_t>(B) * bstride, row, 4});
+    for (int g = 0; g < U; ++g)
+      // out[b, t, hoff[g] + h, :] <- group g row (b, t), real heads only
+      cs->push_back(SegCopy{src[i] + g * B * bstride, dst[i] + static_cast<int64_t>(hoff[g]) * D, 1, 1, B, S, 0, 0,
+                            bstride, row, static_cast<int64_t>(hlen[g]) * D, 4, 0, 0,
+                            static_cast<int64_t>(S) * H * D, static_cast<int64_t>(H) * D});
 }
 
 }  // namespace
@@ -925,7 +960,7 @@ int cp_attention_bwd_launch_count(int B, int H, int S, int D, int ring_degree, i
   if (B <= 0 || S <= 0 || H < 1 || D < 1 || ring_degree < 1 || ulysses_degree < 1) return 0;
   const int U = ulysses_degree;
   int n = 3;  // delta, then the dk/dv and dq kernels (tensor cores for bf16, CUDA cores for fp32)
-  if (U > 1 && H % U == 0) {
+  if (U > 1 && U <= H) {
     const BwdWs w = bwd_ws_layout(B, H, S, D, U, dt);
     char* base = reinterpret_cast<char*>(uintptr_t{1} << 20);
     const void* src[4] = {base, base, base, base};
@@ -1013,7 +1048,7 @@ cp_status cp_attention_bwd(const void* q, const void* k, const void* v, const fl
     return run(B, H);
   }
   // Ulysses / unified: regroup to head groups, the ring backward per group, regroup back
-  const int eb = elem_size(dt), Hg = H / U;
+  const int eb = elem_size(dt), Hg = (H + U - 1) / U;
   const void* src[4] = {q, k, v, dout};
   void* dst[4] = {ws + w.qh, ws + w.kh, ws + w.vh, ws + w.doh};
   float* lh = reinterpret_cast<float*>(ws + w.lh);
@@ -1026,6 +1061,10 @@ cp_status cp_attention_bwd(const void* q, const void* k, const void* v, const fl
   float* gv = reinterpret_cast<float*>(ws + w.dvh);
   a.B = B * U;
   a.H = Hg;
+  if (H % U != 0) {  // Ulysses Anything: short head groups' last slot is padding
+    a.hv_bpg = B;
+    a.hv_short_from = H % U;
+  }
   a.q = dst[0];
   a.k = dst[1];
   a.v = dst[2];

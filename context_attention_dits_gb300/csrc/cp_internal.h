@@ -105,7 +105,17 @@ struct BwdArgs {
   // tensor-core kernels: device error word and the bound on each device-side wait
   uint32_t* err;
   uint64_t timeout_ns;
+  // ragged head groups (Ulysses Anything), as in AttnArgs: batch entries come
+  // in groups of hv_bpg, and groups from hv_short_from on have H - 1 real
+  // heads; head H - 1 of those is padding that no kernel touches.
+  // hv_bpg = 0: no padding.
+  int hv_bpg;
+  int hv_short_from;
 };
+
+__host__ __device__ inline bool bwd_head_is_padding(const BwdArgs& a, int h, int b) {
+  return a.hv_bpg > 0 && h == a.H - 1 && b / a.hv_bpg >= a.hv_short_from;
+}
 constexpr int kBwdTcTile = 128;  // tensor-core backward: keys or query rows per CTA and per step
 
 // Launchers (each returns the launch error, cudaSuccess if none).

@@ -338,7 +338,7 @@ size_t cp_attention_bwd_workspace_size(int B, int H, int S, int D, int ring_degr
  * Ulysses regroups). 0 for empty or invalid sizes. */
 int cp_attention_bwd_launch_count(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt);
 
-/* Backward of cp_attention_fwd (ring, Ulysses or unified).
+/* Backward of cp_attention_fwd (ring, Ulysses, unified or Ulysses Anything).
  *   q, k, v, dout : device [B, S, H, D] of dt (bf16 or fp32), dense;
  *   out, lse      : the forward's results, fp32 [B, S, H, D] and [B, H, S];
  *   dq, dk, dv    : device fp32 [B, S, H, D], written (not accumulated);
@@ -348,9 +348,11 @@ int cp_attention_bwd_launch_count(int B, int H, int S, int D, int ring_degree, i
  * for their products), fp32 accumulation. fp32 runs on the CUDA cores in
  * fp32 throughout. Results are deterministic (no atomics). Asynchronous on
  * `stream`.
- * Errors (returned before any launch): the checks of cp_attention_validate
- * with uneven_ok = 0; uneven_ok != 0 -> CP_ERR_UNSUPPORTED_COMBO (the
- * Anything variants have no backward); a null pointer or non-finite scale ->
+ * uneven_ok selects Ulysses Anything (ulysses_degree > 1, ring_degree == 1:
+ * balanced ragged token shards and head groups, as in cp_attention_fwd).
+ * Errors (returned before any launch): the checks of cp_attention_validate;
+ * uneven_ok != 0 with ring_degree > 1 -> CP_ERR_UNSUPPORTED_COMBO (Ring
+ * Anything is inference only); a null pointer or non-finite scale ->
  * CP_ERR_INVALID_ARG; a pointer not 16-byte aligned -> CP_ERR_ALIGNMENT;
  * workspace missing or short -> CP_ERR_WORKSPACE; launch failure ->
  * CP_ERR_CUDA. B == 0 or S == 0 returns CP_OK without launching. */

@@ -498,6 +498,23 @@ def ring_attention_bwd(q, k, v, dout, scale: float, ring_degree: int, out=None, 
     return dq, dk, dv
 
 
+def ulysses_anything_attention_bwd(q, k, v, dout, scale: float, ulysses_degree: int, out, lse):
+    """Backward of ``ulysses_anything_attention``: the ragged regroups of q, k,
+    v, dout and out (R15), the one-block backward inside each head group with
+    the group's slice of lse, and the inverse regroup of dq, dk and dv."""
+    q, k, v, dout, out, lse = (_f64(t) for t in (q, k, v, dout, out, lse))
+    B, S, H, D = q.shape
+    U = ulysses_degree
+    seq, heads = balanced_split(S, U), balanced_split(H, U)
+    qh, kh, vh, gh, oh = (anything_seq2head([t[:, so:so + sl] for so, sl in seq]) for t in (q, k, v, dout, out))
+    grads = [[], [], []]
+    for g, (ho, hl) in enumerate(heads):
+        res = attention_bwd(qh[g], kh[g], vh[g], gh[g], scale, lse[:, ho:ho + hl, :], attention_delta(oh[g], gh[g]))
+        for i in range(3):
+            grads[i].append(res[i])
+    return tuple(np.concatenate(anything_head2seq(gr), axis=1) for gr in grads)
+
+
 def cp_attention_bwd(q, k, v, dout, scale: float, ring_degree: int = 1, ulysses_degree: int = 1,
                      uneven_ok: bool = False, out=None, lse=None):
     """Backward of ``cp_attention`` for the training variants (R18).
@@ -505,19 +522,26 @@ def cp_attention_bwd(q, k, v, dout, scale: float, ring_degree: int = 1, ulysses_
     Ring: the backward lap above. Ulysses / Unified: the forward's all-to-all
     regroups of q, k, v, dout, out and lse (lse head slices), the ring
     backward inside each head group (ring degree 1 for plain Ulysses), and the
-    inverse regroup of dq, dk and dv. The Anything variants raise
-    UnsupportedComboError: Ring Anything is inference only ([CP] variants
-    table), and Ulysses Anything is left to the forward (reading R19).
+    inverse regroup of dq, dk and dv. Ulysses Anything: the same over ragged
+    token shards and head groups (R15). Ring Anything raises
+    UnsupportedComboError: it is inference only ([CP] variants table and the
+    note closing its section; reading R19).
     """
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     B, S, H, D = q.shape
     R, U = ring_degree, ulysses_degree
     if R < 1 or U < 1:
         raise ValueError("degrees must be >= 1")
-    if uneven_ok:
-        raise UnsupportedComboError("the Anything variants have no backward")
+    if uneven_ok and (R > 1) == (U > 1):
+        raise UnsupportedComboError("an Anything variant needs exactly one of ring_degree, ulysses_degree > 1")
+    if uneven_ok and R > 1:
+        raise UnsupportedComboError("Ring Anything is inference only")
     if U > H:
         raise ValueError(f"ulysses_degree {U} exceeds the number of heads {H}")
+    if uneven_ok:
+        if out is None:
+            out, lse = ulysses_anything_attention(q, k, v, scale, U)
+        return ulysses_anything_attention_bwd(q, k, v, dout, scale, U, out, lse)
     if S % R:
         raise NotDivisibleError(f"sequence length {S} is not divisible by ring_degree {R}")
     if out is None:

@@ -181,13 +181,16 @@ def test_bwd_sizes_counts_and_rejects_before_launch():
     # Ulysses: q, k, v, dout, lse, delta regroups share a launch, dq, dk, dv another
     assert c(1, 24, 4608, 128, 1, 4, torch.bfloat16) == 5
     assert c(0, 24, 4608, 128, 4, 1, torch.bfloat16) == 0
+    # Ulysses Anything over 5 head groups: 30 ragged in-copies (two bulk launches of <= 24), 15 out-copies
+    assert c(1, 24, 4608, 128, 1, 5, torch.bfloat16) == 3 + 2 + 1
     # q, k, v, out, dout, lse, dq, dk, dv, B, H, S, D, scale, R, U, ev, ws, ws_bytes, dt, stream
     big = 1 << 34
     f = lambda **kw: L.cp_attention_bwd(kw.get("q", p), p, p, p, p, p, p, p, kw.get("dv", p), 1, 24,
                                         kw.get("S", 4608), kw.get("D", 128), kw.get("scale", 0.088), kw.get("R", 4),
                                         kw.get("U", 1), kw.get("ev", 0), kw.get("ws", p), kw.get("wsb", big), 0, None)
     assert f(ev=1, S=4607, R=3) == _lib.CP_ERR_UNSUPPORTED_COMBO   # Ring Anything: inference only
-    assert f(ev=1, U=4, R=1) == _lib.CP_ERR_UNSUPPORTED_COMBO
+    assert f(ev=1, S=4481, U=5, R=1, ws=0) == _lib.CP_ERR_WORKSPACE  # Ulysses Anything passes validation
+    assert f(ev=1, U=2, R=2) == _lib.CP_ERR_UNSUPPORTED_COMBO
     assert f(S=4607) == _lib.CP_ERR_NOT_DIVISIBLE
     assert f(D=96) == _lib.CP_ERR_INVALID_ARG
     assert f(scale=float("inf")) == _lib.CP_ERR_INVALID_ARG

@@ -55,33 +55,37 @@ def check(got, want, what, dtype):
     assert rl <= rel_tol, f"{what}: rel L2 {rl:.3e} > {rel_tol}"
 
 
-def run_bwd(q, k, v, out, dout, lse, scale, R, U):
+def run_bwd(q, k, v, out, dout, lse, scale, R, U, ev=False):
     dev = [t.cuda() for t in (q, k, v, out, dout, lse)]
     grads = [torch.empty(q.shape, dtype=torch.float32, device="cuda") for _ in range(3)]
-    cpa().cp_attention_bwd(*dev, *grads, scale, R, U)
+    cpa().cp_attention_bwd(*dev, *grads, scale, R, U, uneven_ok=ev)
     torch.cuda.synchronize()
     return [g.cpu().numpy() for g in grads]
 
 
-@pytest.mark.parametrize("B,S,H,D,R,U,dtype", [
-    (1, 300, 2, 64, 1, 1, "f32"),      # single block, ragged last tile (300 = 4 x 64 + 44)
-    (2, 256, 4, 128, 2, 1, "bf16"),    # ring 2, two batch entries
-    (1, 387, 3, 128, 3, 1, "bf16"),    # ring 3 over 129-token shards: a 1-row tile per shard
-    (1, 512, 4, 64, 1, 2, "bf16"),     # Ulysses 2
-    (2, 384, 4, 128, 2, 2, "f32"),     # unified 2 x 2
-    (1, 1, 1, 128, 1, 1, "bf16"),      # one token: dq = dk = 0, dv = dout
+@pytest.mark.parametrize("B,S,H,D,R,U,ev,dtype", [
+    (1, 300, 2, 64, 1, 1, False, "f32"),      # single block, ragged last tile (300 = 4 x 64 + 44)
+    (2, 256, 4, 128, 2, 1, False, "bf16"),    # ring 2, two batch entries
+    (1, 387, 3, 128, 3, 1, False, "bf16"),    # ring 3 over 129-token shards: a 1-row tile per shard
+    (1, 512, 4, 64, 1, 2, False, "bf16"),     # Ulysses 2
+    (2, 384, 4, 128, 2, 2, False, "f32"),     # unified 2 x 2
+    (1, 1, 1, 128, 1, 1, False, "bf16"),      # one token: dq = dk = 0, dv = dout
+    (1, 1000, 5, 128, 1, 4, True, "bf16"),    # Ulysses Anything: heads 2/1/1/1, tokens 250 x 4
+    (2, 333, 7, 128, 1, 3, True, "bf16"),     # Ulysses Anything: heads 3/2/2, tokens 111 x 3
+    (2, 97, 6, 64, 1, 4, True, "f32"),        # Ulysses Anything on the CUDA cores: heads 2/2/1/1, tokens 25/24/24/24
 ])
-def test_bwd_matches_oracle(B, S, H, D, R, U, dtype):
+def test_bwd_matches_oracle(B, S, H, D, R, U, ev, dtype):
     q, k, v = make_qkv(B, H, S, D, dtype, seed=40 + S)
     dout = make_dout(B, S, H, D, dtype, seed=40 + S)
     scale = D ** -0.5
-    out, lse = co.cp_attention(q, k, v, scale, R, U)
+    out, lse = co.cp_attention(q, k, v, scale, R, U, ev)
     out32 = torch.from_numpy(out).float()
     lse32 = torch.from_numpy(lse).float()
-    want = co.cp_attention_bwd(q, k, v, dout, scale, R, U, out=out32.double().numpy(), lse=lse32.double().numpy())
-    got = run_bwd(q, k, v, out32, dout, lse32, scale, R, U)
+    want = co.cp_attention_bwd(q, k, v, dout, scale, R, U, ev, out=out32.double().numpy(),
+                               lse=lse32.double().numpy())
+    got = run_bwd(q, k, v, out32, dout, lse32, scale, R, U, ev)
     for name, g, w in zip(("dq", "dk", "dv"), got, want):
-        check(g, w, f"{name} B{B} S{S} H{H} D{D} R{R} U{U} {dtype}", dtype)
+        check(g, w, f"{name} B{B} S{S} H{H} D{D} R{R} U{U} ev{int(ev)} {dtype}", dtype)
 
 
 def test_bwd_flux_ring4_sampled():
@@ -119,7 +123,7 @@ def test_bwd_flux_ring4_sampled():
     check(dv[:, idx], gv, "dv sampled keys", "bf16")
 
 
-def test_bwd_rejects_anything_variants():
+def test_bwd_rejects_ring_anything():
     q = torch.zeros((1, 8, 2, 64), dtype=torch.bfloat16, device="cuda")
     o = torch.zeros((1, 8, 2, 64), dtype=torch.float32, device="cuda")
     lse = torch.zeros((1, 2, 8), dtype=torch.float32, device="cuda")

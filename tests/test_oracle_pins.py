@@ -664,14 +664,26 @@ def test_bwd_decompositions_equal_full_backward(R, U, S, H):
         np.testing.assert_allclose(a, b, atol=1e-12, rtol=0)
 
 
-def test_bwd_rejects_anything_and_uneven():
+def test_bwd_rejects_ring_anything_and_uneven():
     q = rnd((1, 7, 2, 2), 290)
     with pytest.raises(co.UnsupportedComboError):
-        co.cp_attention_bwd(q, q, q, q, 0.5, 2, 1, True)
+        co.cp_attention_bwd(q, q, q, q, 0.5, 2, 1, True)     # Ring Anything: inference only
     with pytest.raises(co.UnsupportedComboError):
-        co.cp_attention_bwd(q, q, q, q, 0.5, 1, 2, True)
+        co.cp_attention_bwd(q, q, q, q, 0.5, 2, 2, True)     # Anything with both degrees
     with pytest.raises(co.NotDivisibleError):
         co.cp_attention_bwd(q, q, q, q, 0.5, 2, 1, False)
+
+
+@pytest.mark.parametrize("U,S,H", [(2, 7, 3), (4, 9, 5), (3, 2, 4), (5, 13, 5)])
+def test_bwd_ulysses_anything_equals_full_backward(U, S, H):
+    # ragged token shards and head groups (and a shard with no token when S < U)
+    B, D, scale = 2, 3, 0.7
+    q, k, v, dout = (rnd((B, S, H, D), 320 + i, 1.2) for i in range(4))
+    out, lse = co.attention(q, k, v, scale)
+    full = co.attention_bwd(q, k, v, dout, scale, lse, co.attention_delta(out, dout))
+    got = co.cp_attention_bwd(q, k, v, dout, scale, 1, U, True)
+    for a, b in zip(got, full):
+        np.testing.assert_allclose(a, b, atol=1e-12, rtol=0)
 
 
 def _mut_bwd(kind):
@@ -733,3 +745,19 @@ def test_planted_bwd_lap_mistake_is_caught():
                                         lse[:, :, qo:qo + ql], delta[:, :, qo:qo + ql])
             dq[:, qo:qo + ql] += gq
     assert np.max(np.abs(dq - full[0])) > 1e-6
+
+
+def test_planted_anything_bwd_lse_slice_mistake_is_caught():
+    # a Ulysses Anything backward that hands every head group the first groups' lse rows
+    B, S, H, D, U, scale = 1, 9, 5, 3, 4, 0.7
+    q, k, v, dout = (rnd((B, S, H, D), 330 + i, 1.2) for i in range(4))
+    out, lse = co.attention(q, k, v, scale)
+    full = co.attention_bwd(q, k, v, dout, scale, lse, co.attention_delta(out, dout))
+    seq, heads = co.balanced_split(S, U), co.balanced_split(H, U)
+    qh, kh, vh, gh, oh = (co.anything_seq2head([t[:, so:so + sl] for so, sl in seq]) for t in (q, k, v, dout, out))
+    dq = []
+    for g, (ho, hl) in enumerate(heads):
+        res = co.attention_bwd(qh[g], kh[g], vh[g], gh[g], scale, lse[:, 0:hl, :], co.attention_delta(oh[g], gh[g]))
+        dq.append(res[0])
+    bad = np.concatenate(co.anything_head2seq(dq), axis=1)
+    assert np.max(np.abs(bad - full[0])) > 1e-6
