@@ -79,10 +79,10 @@ constexpr int kF32RowsPerCta = 8;
 inline int f32_items_for_rows(int rows) { return (rows + kF32RowsPerCta - 1) / kF32RowsPerCta; }
 
 // Backward of a ring lap over n even shards of one sequence (query shards and
-// K/V blocks share the table). q, k, v, dout and the outputs dq, dk, dv are
+// K/V blocks share the table; n = 1 for Ulysses and Ulysses Anything). q, k, v, dout and the outputs dq, dk, dv are
 // [B, S, H, D] with element strides (bstride, sstride, 1 per head of D);
 // lse and delta are [B, H, S] with batch stride l_bstride.
-constexpr int kBwdTile = 64;  // query rows per dq CTA, keys per dk/dv CTA
+constexpr int kBwdTile = 64;  // CUDA-core backward: query rows per dq CTA, keys per dk/dv CTA
 struct BwdArgs {
   int n;
   int off[kMaxRanks];
@@ -148,12 +148,14 @@ struct SegCopy {
   int elem_bytes;
   int64_t ost0, ost1, ost2, ost3;
 };
-// Picks the widest vector (16, 8, 4 or 1 bytes) that every segment start, the
+// One copy: the bulk path when it qualifies (see launch_segment_copies), else
+// the widest vector (16, 8, 4 or 1 bytes) that every segment start, the
 // segment length and both base pointers allow.
 cudaError_t launch_segment_copy(const SegCopy& c, cudaStream_t s);
-// n copies in stream order of launches: the copies that take the bulk path
-// (16-byte aligned, segments of 256 B to 24 KB) share launches, up to 24 per
-// launch; every other copy takes a launch of its own.
+// n independent copies (no copy reads what another writes; a launch runs its
+// copies concurrently): the ones that take the bulk path (16-byte aligned,
+// segments of 256 B to 24 KB) share launches, up to 24 per launch; every
+// other copy takes a vector launch of its own.
 cudaError_t launch_segment_copies(const SegCopy* cs, int n, cudaStream_t s);
 // The number of launches launch_segment_copies makes for the same copies
 // (pointers need only carry their alignment).

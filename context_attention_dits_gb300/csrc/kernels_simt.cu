@@ -5,7 +5,8 @@
 //     (bandwidth-bound, 128-bit loads and stores);
 //   * the segment copy behind the Ulysses seq<->head regroups (bandwidth-bound):
 //     bulk TMA copies through a shared-memory ring when segments are 16-byte
-//     multiples of a few hundred bytes or more, else warps of 128-bit vectors.
+//     multiples of a few hundred bytes or more (up to 24 independent copies
+//     per launch), else warps of 128-bit vectors.
 #include <cuda_runtime.h>
 
 #include <cmath>
