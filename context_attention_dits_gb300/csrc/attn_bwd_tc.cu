@@ -376,10 +376,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // dq: one CTA per 128 query rows of one (batch entry, head); Q and dO loaded
 // once, K and V tiles of the rank's lap streamed in ring order ((r - t) mod n)
 // through two stages. Per K/V tile three MMAs (M = 128 query rows):
-//   S  = Q K^T    (SS, both K-major)                     -> TMEM [0, 128)
+//   S  = Q K^T    (SS, both K-major)                     -> TMEM [0, 128) or [384, 512)
 //   dP = dO V^T   (SS)                                   -> TMEM [128, 256)
 //   dQ += dS K    (TS: dS in TMEM over S's consumed columns, K read MN-major)
 //                                                        -> TMEM [256, 256 + D)
+// S alternates between its two slots, so the next tile's S is computed while
+// the row pass works on this tile; dP, read by the same pass, has one slot.
 // Warps 2-5 (one thread per query row, lse and delta in registers) form
 // dS = p (dp - delta) between the first two and the third. dq is stored once,
 // without atomics.
@@ -543,34 +545,60 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       if (leader) mma_commit(bar_addr);
     };
     auto kstep = [](int kk) -> uint32_t { return static_cast<uint32_t>(((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4); };
-    bool ok = mbar_wait_bounded(bar(kDqBarQ), 0, abort_flag, a.err, tmo);
-    for (int it = 0; ok && it < NT; ++it) {
-      const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      const uint32_t stage = static_cast<uint32_t>((s * L::kTile) >> 4);
-      if (!mbar_wait_bounded(bar(kDqBarKVFull + s), ph, abort_flag, a.err, tmo)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+    // S of tile it lives in TMEM [0, 128) for even it, [384, 512) for odd it, so
+    // the next tile's S = Q K^T runs while the row pass works on this tile's
+    auto wait_kv = [&](int it) -> bool {
+      return mbar_wait_bounded(bar(kDqBarKVFull + (it & 1)), (it >> 1) & 1, abort_flag, a.err, tmo);
+    };
+    auto issue_s = [&](int it) {
+      const uint32_t stage = static_cast<uint32_t>(((it & 1) * L::kTile) >> 4);
+      const uint32_t d_tmem = tmem + ((it & 1) ? 384u : 0u);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        if (leader) mma_ss_lohi(tmem, q_lo + kstep(kk), km_hi, k_lo + stage + kstep(kk), km_hi, idesc_s, kk > 0);
+        if (leader) mma_ss_lohi(d_tmem, q_lo + kstep(kk), km_hi, k_lo + stage + kstep(kk), km_hi, idesc_s, kk > 0);
+    };
+    auto issue_dp = [&](int it) {
+      const uint32_t stage = static_cast<uint32_t>(((it & 1) * L::kTile) >> 4);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         if (leader) mma_ss_lohi(tmem + 128, o_lo + kstep(kk), km_hi, v_lo + stage + kstep(kk), km_hi, idesc_s, kk > 0);
+    };
+    bool ok = mbar_wait_bounded(bar(kDqBarQ), 0, abort_flag, a.err, tmo) && (NT == 0 || wait_kv(0));
+    if (ok && NT > 0) {
+      tc_fence_after();
+      issue_s(0);
+      issue_dp(0);
       commit(bar(kDqBarSFull));
+    }
+    for (int it = 0; ok && it < NT; ++it) {
+      const int s = it & 1;
+      const uint32_t stage = static_cast<uint32_t>((s * L::kTile) >> 4);
+      // the next tile's S: its slot's last reader (dQ of tile it - 1) is already issued
+      if (it + 1 < NT) {
+        if (!wait_kv(it + 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_s(it + 1);
+      }
       if (!mbar_wait_bounded(bar(kDqBarPFull), it & 1, abort_flag, a.err, tmo)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // dQ += dS K   (K = keys: 16 key rows = 2048 bytes of the MN-major K tile)
+      // dQ += dS K   (dS over S's first 64 columns; K = keys: 16 key rows = 2048 bytes of the MN-major K tile)
+      const uint32_t a_tmem = tmem + (s ? 384u : 0u);
 #pragma unroll
       for (int kk = 0; kk < kT / 16; ++kk)
-        if (leader) mma_ts_lohi(tmem + 256, tmem + kk * 8, k_mn_lo + stage + ((kk * 2048) >> 4), mn_hi, idesc_q,
+        if (leader) mma_ts_lohi(tmem + 256, a_tmem + kk * 8, k_mn_lo + stage + ((kk * 2048) >> 4), mn_hi, idesc_q,
                                 (it > 0 || kk > 0) ? 1u : 0u);
       commit(bar(kDqBarKVEmpty + s));
+      // the next tile's dP, now that the row pass has read this one
+      if (it + 1 < NT) {
+        issue_dp(it + 1);
+        commit(bar(kDqBarSFull));
+      }
     }
     if (ok) {
       commit(bar(kDqBarDone));
@@ -583,7 +611,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
+    const uint32_t t_dp = tmem + lane_off + 128;
     const float c2 = a.scale * kLog2eB;
     // the row's lse (times log2 e) and delta; a row past the shard, or one that
     // saw no key, gets lse = +inf so that p = 0
@@ -601,6 +629,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kDqBarSFull), it & 1, abort_flag, a.err, tmo));
       if (!ok) break;
       tc_fence_after();
+      const uint32_t t_s = tmem + lane_off + ((it & 1) ? 384u : 0u);  // this tile's S slot
       const int nvk = cur.nvalid();
 #pragma unroll 1
       for (int c = 0; c < kT / 32; ++c) {
