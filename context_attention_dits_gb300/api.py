@@ -257,8 +257,9 @@ def cp_attention_bwd(q, k, v, out, dout, lse, dq, dk, dv, scale: float, ring_deg
     """Backward of cp_attention_fwd: q, k, v, dout [B,S,H,D] (one dtype), out [B,S,H,D] f32 and
     lse [B,H,S] f32 from the forward -> dq, dk, dv [B,S,H,D] f32 (written).
 
-    workspace: a CUDA uint8 tensor of at least cp_attention_bwd_workspace_size(...) bytes;
-    allocated here through torch when None.
+    Ring, Ulysses, unified, and Ulysses Anything (uneven_ok with ulysses_degree > 1); Ring
+    Anything is inference only and raises. workspace: a CUDA uint8 tensor of at least
+    cp_attention_bwd_workspace_size(...) bytes; allocated here through torch when None.
     """
     _cuda(q, k, v, out, dout, lse, dq, dk, dv)
     B, S, H, D = q.shape
