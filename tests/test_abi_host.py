@@ -204,3 +204,10 @@ def test_bwd_sizes_counts_and_rejects_before_launch():
     assert f(ws=0) == _lib.CP_ERR_WORKSPACE
     assert f(wsb=16) == _lib.CP_ERR_WORKSPACE
     assert f(ws=p + 16) == _lib.CP_ERR_ALIGNMENT
+    # empty problems launch nothing and succeed
+    assert L.cp_attention_bwd(p, p, p, p, p, p, p, p, p, 0, 24, 4608, 128, 0.088, 4, 1, 0, None, 0, 0, None) == 0
+    assert L.cp_attention_bwd(p, p, p, p, p, p, p, p, p, 1, 24, 0, 128, 0.088, 1, 4, 0, None, 0, 0, None) == 0
+    # ragged head groups are stored padded: 24 heads over 5 groups take 5 x 5 head slots
+    hp = 25
+    assert ws(1, 24, 4608, 128, 1, 5, torch.bfloat16) >= nl * 4 + 4 * (n // 24 * hp) * 2 + 2 * (nl // 24 * hp) * 4 \
+        + 3 * (n // 24 * hp) * 4
