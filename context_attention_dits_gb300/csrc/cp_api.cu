@@ -837,6 +837,11 @@ extern "C" cp_status cp_attention_fwd_no_alloc(const void* q, const void* k, con
   if (B == 0 || S == 0) return CP_OK;
   DeviceInfo* dev = nullptr;
   if ((st = current_device(&dev)) != CP_OK) return st;
+  // a problem that needs no scratch (plain ring, fused lap) never touches the
+  // array, so it neither looks the symbol up nor makes a first-call set-up
+  if (need == 0)
+    return cp_attention_fwd(q, k, v, out, lse, B, H, S, D, scale, ring_degree, ulysses_degree, uneven_ok, nullptr, 0,
+                            dt, mode, stream);
   void* ws = nullptr;
   if ((st = no_alloc_workspace(&ws)) != CP_OK) return st;
   return cp_attention_fwd(q, k, v, out, lse, B, H, S, D, scale, ring_degree, ulysses_degree, uneven_ok, ws,

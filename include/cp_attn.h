@@ -20,7 +20,10 @@
  *     of exp over the scaled logits scale * q.k. Non-causal, no mask.
  *   - Pointers are DEVICE pointers unless stated. The caller owns every buffer
  *     (inputs, outputs, workspace); the library allocates no device memory
- *     and keeps no per-call state. Outputs must not alias inputs unless stated.
+ *     and keeps no per-call state. The one exception is
+ *     cp_attention_fwd_no_alloc, whose built-in 64 MiB static device array
+ *     (CP_NO_ALLOC_WORKSPACE_BYTES) is shared by all of its calls. Outputs
+ *     must not alias inputs unless stated.
  *   - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Every call is asynchronous on that stream. Arguments are validated on
  *     the host before anything is launched; a failed validation launches
@@ -297,9 +300,11 @@ cp_status cp_debug_bounded_wait_probe(int timeout_us, void* stream);
  * cp_attention_fwd minus the workspace, and uses instead a workspace of
  * CP_NO_ALLOC_WORKSPACE_BYTES (64 MiB) that the library holds as a static
  * device array: every GPU that loads the library keeps those 64 MiB until the
- * process exits. The first call on a device looks the array's device address
- * up (once per device, with that device current); make that first call
- * before any stream capture. No part of the array needs to start at zero
+ * process exits. The first call on a device that needs scratch memory looks
+ * the array's device address up (once per device, with that device current);
+ * make that first call before any stream capture. A call that needs no
+ * scratch (cp_attention_workspace_size(...) == 0, e.g. a plain ring with the
+ * fused lap) never touches the array. No part of the array needs to start at zero
  * (every byte used is written before it is read), but all calls share it:
  * calls whose work overlaps on the GPU (other streams, other host threads)
  * race on it and must be serialised by the caller. The call allocates no
