@@ -174,14 +174,26 @@ def _time_batch(fns, flush, stream, rounds):
     return sum(a.elapsed_time(b) for a, b in zip(st, en)) / (rounds * len(fns))
 
 
-def secondary(cpa, dev, flush, stream, peaks):
+def secondary(cpa, dev, flush, stream, peaks, clocks=None):
     """Achieved bandwidth of the merge and regroup kernels (algorithmic bytes / event time) and the
-    throughput of cp_attention_fwd on the other workloads."""
+    throughput of cp_attention_fwd on the other workloads. Every line carries the clock summary of its
+    own timed window."""
     import torch
     from synth import WORKLOADS, make_merge_operands, make_qkv
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     res = {}
+    win = {"t0": time.time()}
+
+    def opened():
+        torch.cuda.synchronize()
+        win["t0"] = time.time()
+
+    def closed(name):
+        torch.cuda.synchronize()
+        if clocks is not None and name in res:
+            res[name]["clocks"] = clocks.summary((win["t0"], time.time()))
+        win["t0"] = time.time()
 
     def bw(name, nbytes, ms_single, ms_batch, note):
         res[name] = {"bytes_per_launch": nbytes, "single_launch": {"ms": ms_single, "GB_s": nbytes / ms_single / 1e6,
@@ -189,10 +201,28 @@ def secondary(cpa, dev, flush, stream, peaks):
                      "back_to_back": {"ms": ms_batch, "GB_s": nbytes / ms_batch / 1e6,
                                       "frac_of_hbm": nbytes / ms_batch / 1e6 / hbm},
                      "note": note}
+        closed(name)
+
+    def fwd_line(name, w, ms, launches, **extra):
+        tf = w.flops / (ms * 1e-3) / 1e12
+        res[name] = {"TFLOP_s": tf, "ms": ms, "frac_of_bf16_peak": tf / bf16, "launches": launches, **extra}
+        closed(name)
+
+    # LSE merge at the shape the stepwise FLUX ring-4 lap launches: one ring step's partial of all four
+    # simulated ranks, [1,4608,24,128] fp32 + lse [1,24,4608] (171 MB); the lap runs three of them,
+    # each after that step's attention launch
+    opened()
+    sets = [[t.to(dev) for t in make_merge_operands(1, 24, 4608, 128, seed=15 + i)] for i in range(3)]
+    nbytes = 12 * sets[0][0].numel() + 12 * sets[0][1].numel()
+    fns = [lambda o=o: cpa.cp_lse_merge(o[0], o[1], o[2], o[3], stream=stream) for o in sets]
+    bw("lse_merge_flux_ring4_lap_step", nbytes, _time_events(fns[0], flush, stream, 20),
+       _time_batch(fns, flush, stream, 5), "the launched shape; back_to_back: the lap's three merges")
+    del sets, fns
 
     # LSE merge of one FLUX ring-4 rank-step partial: [1,1152,24,128] fp32 + lse [1,24,1152];
-    # a stepwise lap runs 12 of them. Eight operand sets (342 MB) rotate through the batch.
+    # one rank's share of a lap step's merge. Eight operand sets (342 MB) rotate through the batch.
     B, S, H, D = 1, 1152, 24, 128
+    opened()
     sets = [[t.to(dev) for t in make_merge_operands(B, H, S, D, seed=5 + i)] for i in range(8)]
     nbytes = 12 * sets[0][0].numel() + 12 * sets[0][1].numel()
     fns = [lambda o=o: cpa.cp_lse_merge(o[0], o[1], o[2], o[3], stream=stream) for o in sets]
@@ -204,9 +234,11 @@ def secondary(cpa, dev, flush, stream, peaks):
     # four head groups, [4, 32768, 6, 128] fp32, 402 MB), as the stepwise lap of that workload runs it
     oa, la, ob, lb = (t.to(dev) for t in make_merge_operands(4, 6, 32768, 128, seed=9))
     nbytes = 12 * oa.numel() + 12 * la.numel()
+    opened()
     ms = _time_events(lambda: cpa.cp_lse_merge(oa, la, ob, lb, stream=stream), flush, stream, 10)
     res["lse_merge_video_unified_step"] = {"bytes_per_launch": nbytes, "single_launch": {
         "ms": ms, "GB_s": nbytes / ms / 1e6, "frac_of_hbm": nbytes / ms / 1e6 / hbm}}
+    closed("lse_merge_video_unified_step")
     del oa, la, ob, lb
 
     # Ulysses regroups of FLUX Ulysses-4: q, k, v (bf16) seq->head; out (fp32) head->seq
@@ -214,6 +246,7 @@ def secondary(cpa, dev, flush, stream, peaks):
     xs = [torch.randn((U, 1, S // U, H, D), device=dev).to(torch.bfloat16) for _ in range(6)]
     ys = [torch.empty((U, 1, S, H // U, D), device=dev, dtype=torch.bfloat16) for _ in range(6)]
     nbytes = 2 * xs[0].numel() * 2
+    opened()
     fns = [lambda x=x, y=y: cpa.cp_ulysses_seq2head(x, y, stream=stream) for x, y in zip(xs, ys)]
     bw("seq2head_flux_ulysses4_bf16", nbytes, _time_events(fns[0], flush, stream, 30),
        _time_batch(fns * 2, flush, stream, 5), "one tensor; back_to_back: 12 regroups over 6 tensor pairs")
@@ -221,6 +254,7 @@ def secondary(cpa, dev, flush, stream, peaks):
     xs = [torch.randn((U, 1, S, H // U, D), device=dev) for _ in range(3)]
     ys = [torch.empty((U, 1, S // U, H, D), device=dev) for _ in range(3)]
     nbytes = 2 * xs[0].numel() * 4
+    opened()
     fns = [lambda x=x, y=y: cpa.cp_ulysses_head2seq(x, y, stream=stream) for x, y in zip(xs, ys)]
     bw("head2seq_flux_ulysses4_f32", nbytes, _time_events(fns[0], flush, stream, 30),
        _time_batch(fns * 4, flush, stream, 5), "the fp32 output; back_to_back: 12 regroups over 3 tensor pairs")
@@ -231,11 +265,39 @@ def secondary(cpa, dev, flush, stream, peaks):
     y = torch.empty((4, 1, 32768, 6, 128), device=dev, dtype=torch.bfloat16)
     xr = x.view(1, 4, 8192, 24, 128).permute(1, 0, 2, 3, 4).contiguous()  # four 8192-token rank shards
     nbytes = 2 * x.numel() * 2
+    opened()
     ms = _time_events(lambda: cpa.cp_ulysses_seq2head(xr.view(4, 1, 8192, 24, 128), y.view(4, 1, 32768, 6, 128),
                                                        stream=stream), flush, stream, 10)
     res["seq2head_32768tok_ulysses4_bf16"] = {"bytes_per_launch": nbytes, "single_launch": {
         "ms": ms, "GB_s": nbytes / ms / 1e6, "frac_of_hbm": nbytes / ms / 1e6 / hbm}}
+    closed("seq2head_32768tok_ulysses4_bf16")
     del x, y, xr
+
+    # the stepwise FLUX ring-4 lap as a whole (one attention launch per ring step over all ranks, fp32
+    # partials, the merge after each step but the first), next to the fused lap of the same inputs
+    w = WORKLOADS["flux_ring4"]
+    q, k, v = (t.to(dev) for t in make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed, w.q_mult))
+    out = torch.empty((w.B, w.S, w.H, w.D), device=dev)
+    lse = torch.empty((w.B, w.H, w.S), device=dev)
+    for mode in ("stepwise", "fused"):
+        wsb = cpa.cp_attention_workspace_size(w.B, w.H, w.S, w.D, w.ring_degree, 1, q.dtype, mode)
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+        opened()
+        ms = _time_events(lambda: cpa.cp_attention_fwd(q, k, v, out, lse, w.scale, w.ring_degree, 1, False,
+                                                        workspace=ws, mode=mode, stream=stream), flush, stream, 20)
+        fwd_line(f"flux_ring4_{mode}", w, ms,
+                 cpa.cp_attention_launch_count(w.B, w.H, w.S, w.D, w.ring_degree, 1, q.dtype, mode),
+                 lap_mode=mode)
+        del ws
+    step_part = (w.B * w.S * w.H * w.D + w.B * w.H * w.S) * 4  # one step's fp32 partial (out + lse)
+    extra_bytes = (w.ring_degree - 1) * 4 * step_part  # per later step: partial written, merge reads 2, writes 1
+    extra_ms = res["flux_ring4_stepwise"]["ms"] - res["flux_ring4_fused"]["ms"]
+    res["flux_ring4_stepwise"]["extra_vs_fused"] = {
+        "ms": extra_ms, "algorithmic_bytes": extra_bytes,
+        "GB_s": extra_bytes / extra_ms / 1e6 if extra_ms > 0 else None,
+        "frac_of_hbm": extra_bytes / extra_ms / 1e6 / hbm if extra_ms > 0 else None,
+        "note": "the partials' fp32 write and the merges' reads and write, over the stepwise lap's extra time"}
+    del q, k, v, out, lse
 
     # cp_attention_fwd on the other workloads (fused lap), inputs resident
     for name in ("flux_ulysses4", "ring_anything3", "video_unified", "flux1008_ulysses_anything4",
@@ -246,14 +308,33 @@ def secondary(cpa, dev, flush, stream, peaks):
         lse = torch.empty((w.B, w.H, w.S), device=dev)
         wsb = cpa.cp_attention_workspace_size(w.B, w.H, w.S, w.D, w.ring_degree, w.ulysses_degree, q.dtype, "fused")
         ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+        opened()
         ms = _time_events(lambda: cpa.cp_attention_fwd(q, k, v, out, lse, w.scale, w.ring_degree,
                                                         w.ulysses_degree, w.uneven_ok, workspace=ws,
                                                         mode="fused", stream=stream),
                           flush, stream, 5 if name == "video_unified" else 20)
-        tf = w.flops / (ms * 1e-3) / 1e12
-        res[name] = {"TFLOP_s": tf, "ms": ms, "frac_of_bf16_peak": tf / bf16,
-                     "launches": cpa.cp_attention_launch_count(w.B, w.H, w.S, w.D, w.ring_degree,
-                                                               w.ulysses_degree, q.dtype, "fused")}
+        fwd_line(name, w, ms, cpa.cp_attention_launch_count(w.B, w.H, w.S, w.D, w.ring_degree,
+                                                             w.ulysses_degree, q.dtype, "fused"))
+        if name == "flux_ulysses4":
+            # the same attention launch alone, on head-grouped copies [U*B, S, H/U, D]: what the call adds on
+            # top is the cost of its regroups (q, k, v seq->head; out, lse head->seq)
+            U, Hg = w.ulysses_degree, w.H // w.ulysses_degree
+            qh, kh, vh = (t.view(w.B, w.S, U, Hg, w.D).permute(2, 0, 1, 3, 4).reshape(U * w.B, w.S, Hg, w.D)
+                          .contiguous() for t in (q, k, v))
+            oh = torch.empty((U * w.B, w.S, Hg, w.D), device=dev)
+            lh = torch.empty((U * w.B, Hg, w.S), device=dev)
+            opened()
+            ms_attn = _time_events(lambda: cpa.cp_block_attn_fwd(qh, kh, vh, oh, lh, w.scale, stream=stream),
+                                   flush, stream, 20)
+            rg_bytes = 2 * 3 * q.numel() * q.element_size() + 2 * (out.numel() + lse.numel()) * 4
+            rg_ms = ms - ms_attn
+            res[name]["regroup_cost"] = {
+                "attention_only_ms": ms_attn, "regroups_ms": rg_ms, "regroup_bytes": rg_bytes,
+                "GB_s": rg_bytes / rg_ms / 1e6 if rg_ms > 0 else None,
+                "frac_of_hbm": rg_bytes / rg_ms / 1e6 / hbm if rg_ms > 0 else None,
+                "note": "call time minus the attention launch alone; regroups move 2 x (q, k, v, out, lse)"}
+            closed(name)
+            del qh, kh, vh, oh, lh
         del q, k, v, out, lse, ws
     # key-padding mask: FLUX ring 4 with text keys 300..511 masked (FLOPs counted dense, as unmasked)
     w = WORKLOADS["flux_ring4"]
@@ -262,11 +343,10 @@ def secondary(cpa, dev, flush, stream, peaks):
     lse = torch.empty((w.B, w.H, w.S), device=dev)
     km = torch.ones((w.B, w.S), dtype=torch.bool, device=dev)
     km[:, 300:512] = False
+    opened()
     ms = _time_events(lambda: cpa.cp_attention_fwd(q, k, v, out, lse, w.scale, w.ring_degree, 1, False,
                                                     mode="fused", stream=stream, key_mask=km), flush, stream, 20)
-    tf = w.flops / (ms * 1e-3) / 1e12
-    res["flux_ring4_text_padding_mask"] = {"TFLOP_s": tf, "ms": ms, "frac_of_bf16_peak": tf / bf16, "launches": 1,
-                                           "note": "keys 300..511 masked; FLOPs counted as unmasked"}
+    fwd_line("flux_ring4_text_padding_mask", w, ms, 1, note="keys 300..511 masked; FLOPs counted as unmasked")
     del q, k, v, out, lse, km
 
     # backward of the FLUX ring-4 and Ulysses-4 forwards: algorithmic FLOPs are 2.5x the forward's
@@ -282,12 +362,14 @@ def secondary(cpa, dev, flush, stream, peaks):
         grads = [torch.empty_like(out) for _ in range(3)]
         ws = torch.empty(max(1, cpa.cp_attention_bwd_workspace_size(w.B, w.H, w.S, w.D, R, U, q.dtype)),
                          dtype=torch.uint8, device=dev)
+        opened()
         ms = _time_events(lambda: cpa.cp_attention_bwd(q, k, v, out, dout, lse, *grads, w.scale, R, U,
-                                                       workspace=ws, stream=stream), flush, stream, 3)
+                                                       workspace=ws, stream=stream), flush, stream, 10)
         tf = 2.5 * w.flops / (ms * 1e-3) / 1e12
         res[name] = {"TFLOP_s": tf, "ms": ms, "frac_of_bf16_peak": tf / bf16,
                      "launches": cpa.cp_attention_bwd_launch_count(w.B, w.H, w.S, w.D, R, U, q.dtype),
                      "note": "tensor-core backward (dk/dv and dq kernels); FLOPs = 2.5 x forward"}
+        closed(name)
         del q, k, v, dout, out, lse, grads, ws
     if cpa.cp_check_device_status() != 0:
         raise RuntimeError("device status after the secondary measurements")
@@ -333,10 +415,10 @@ class ClockSampler:
         if self.thread:
             self.thread.join(timeout=5)
 
-    def summary(self):
+    def summary(self, window=None):
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        t0, t1 = self.window or (0, float("inf"))
+        t0, t1 = window or self.window or (0, float("inf"))
         inside = [p for (t, p) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
         if not inside:  # a short timed region: take the samples nearest to it
             mid = 0.5 * (t0 + t1)
@@ -466,12 +548,11 @@ def run_ours(args, w, world, rank, local):
         cpa.cp_attention_fwd(q, k, v, out, lse, w.scale, w.ring_degree, w.ulysses_degree, w.uneven_ok,
                              workspace=ws, mode=mode, stream=stream)
 
-    for _ in range(max(3, args.warmup)):
-        step()
+    step()
     torch.cuda.synchronize()
     status = cpa.cp_check_device_status()
     if status != 0:
-        raise RuntimeError(f"device status after warm-up: {cpa.cp_status_string(status)}")
+        raise RuntimeError(f"device status after the first call: {cpa.cp_status_string(status)}")
 
     # parity spot check of the benchmarked output on a few rows (oracle, rank 0 only)
     parity = None
@@ -497,6 +578,11 @@ def run_ours(args, w, world, rank, local):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
+    # the warm-up steps run right before the timed ones, with the same L2 flush between steps, so that
+    # the timed region starts on a GPU that is already busy with this work
+    for i in range(max(3, args.warmup)):
+        flush.fill_(float(-1 - i))
+        step()
     torch.cuda.synchronize()
     wall0 = time.time()
     for i in range(args.steps):
@@ -577,7 +663,13 @@ def run_ours(args, w, world, rank, local):
             cpu = cpu_baseline(w, q_h, k_h, v_h)
         sec = None
         if world == 1 and not args.no_secondary:
-            sec = secondary(cpa, dev, flush, stream, peaks)
+            sec_clocks = ClockSampler(gpu_id)
+            time.sleep(0.3)
+            try:
+                sec = secondary(cpa, dev, flush, stream, peaks, sec_clocks)
+            finally:
+                time.sleep(0.25)
+                sec_clocks.stop()
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
