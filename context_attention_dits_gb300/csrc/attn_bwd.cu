@@ -405,7 +405,35 @@ cudaError_t launch_delta_d(const float* out, const void* dout, float* delta, int
   return cudaGetLastError();
 }
 
+// lse * log2 e and delta of every shard's rows into the padded per-shard
+// layout of BwdArgs::lse2p / dltp: element (bh, r, i) for i < lpad.
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constant__ BwdArgs a) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  const int64_t per_bh = static_cast<int64_t>(a.n) * a.lpad;
+  if (idx >= static_cast<int64_t>(a.B) * a.H * per_bh) return;
+  const int64_t bh = idx / per_bh;
+  const int rem = static_cast<int>(idx - bh * per_bh);
+  const int r = rem / a.lpad, i = rem - r * a.lpad;
+  float l2 = INFINITY, dl = 0.f;  // padding: p = 0
+  if (i < a.len[r]) {
+    const int64_t b = bh / a.H, h = bh - b * a.H;
+    const int64_t o = b * a.l_bstride + h * a.S + a.off[r] + i;
+    const float l = a.lse[o];
+    l2 = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;  // a row that saw no key: p = 0
+    dl = a.delta[o];
+  }
+  a.lse2p[idx] = l2;
+  a.dltp[idx] = dl;
+}
+
 }  // namespace
+
+cudaError_t launch_attn_bwd_prep(const BwdArgs& a, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(a.B) * a.H * a.n * a.lpad;
+  if (n == 0) return cudaSuccess;
+  attn_bwd_prep_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attn_bwd(const BwdArgs& a, int D, bool bf16, cudaStream_t s) {
   if (D == 128) return bf16 ? launch_bwd_d<128, __nv_bfloat16>(a, s) : launch_bwd_d<128, float>(a, s);

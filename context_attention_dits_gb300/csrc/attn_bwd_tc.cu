@@ -6,24 +6,32 @@
 //   p_ij = exp(scale q_i.k_j - lse_i),  ds_ij = p_ij (dout_i.v_j - delta_i),
 //   dv_j = sum_i p_ij dout_i,  dk_j = scale sum_i ds_ij q_i,  dq_i = scale sum_j ds_ij k_j.
 //
-// Two kernels, neither with atomics:
+// Two kernels, neither with atomics, each walking its lap in 64-row
+// sub-steps whose S / dP pair alternates between two TMEM slots, so that the
+// row pass of one sub-step runs while the tensor cores work on the other's:
 //
 // dk / dv: one CTA owns a tile of 128 keys of one (batch entry, head) and
-// walks every 128-row query tile of the lap, rank by rank in the order its
-// K/V block visits them ((j + t) mod n). Per query tile, four MMAs (M = 128):
-//   1. S^T  = K Q^T      (A = K tile, B = Q tile; both K-major)  -> TMEM [0, 128)
-//   2. dP^T = V dO^T     (A = V tile, B = dO tile)               -> TMEM [128, 256)
-//   3. dV  += P^T dO     (A = P^T in TMEM, B = dO MN-major)      -> TMEM [256, 256 + D)
-//   4. dK  += dS^T Q     (A = dS^T in TMEM, B = Q MN-major)      -> TMEM [256 + D, 256 + 2D)
-// Between 2 and 3 the softmax warpgroup (one thread per key row) turns S^T
-// and dP^T into P^T (bf16, over S^T's first 64 columns) and dS^T (bf16, over
-// dP^T's first 64 columns). After the last query tile it writes dk and dv.
+// walks every 64-row query sub-tile of the lap, rank by rank in the order its
+// K/V block visits them ((j + t) mod n). Per sub-tile, four MMAs (M = 128):
+//   1. S^T  = K Q^T      (A = K tile, B = Q sub-tile; both K-major; N = 64)
+//   2. dP^T = V dO^T     (A = V tile, B = dO sub-tile)
+//   3. dV  += P^T dO     (A = P^T in TMEM, B = dO MN-major; K = 64 rows)
+//   4. dK  += dS^T Q     (A = dS^T in TMEM, B = Q MN-major)
+// S^T and dP^T of sub-step j sit in TMEM slot j mod 2 (columns [0, 64) and
+// [64, 128) of the slot); dV and dK in [256, 256 + D) and [256 + D, 256 + 2D).
+// Between 2 and 3 the row warpgroup (one thread per key row) turns S^T and
+// dP^T into P^T and dS^T (bf16, over the first 32 columns of each). The MMAs
+// 1 and 2 of sub-step j + 2 are issued right after 3 and 4 of sub-step j, so
+// they run while the row pass works on sub-step j + 1. Q, dO, lse and delta
+// stream through four 64-row slots. After the last sub-tile it writes dk, dv.
 //
-// dq: one CTA owns 128 query rows and walks the K/V tiles of its rank's lap
-// in ring order ((r - t) mod n): S = Q K^T, dP = dO V^T, then dQ += dS K with
-// dS (a thread per query row) in TMEM over S's consumed columns; dq is
-// stored once. It recomputes S and dP, 1.4x the MMA work of a single fused
-// kernel, in exchange for no reduction of dq tiles across key-tile CTAs.
+// dq: one CTA owns 128 query rows (Q and dO loaded once) and walks the
+// 64-key K/V sub-tiles of its rank's lap in ring order ((r - t) mod n):
+// S = Q K^T and dP = dO V^T (N = 64) into TMEM slot j mod 2, then dQ += dS K
+// with dS (a thread per query row) over S's first 32 columns; dq is stored
+// once. It recomputes S and dP, 1.4x the MMA work of a single fused kernel,
+// in exchange for no reduction of dq tiles across key-tile CTAs. K and V
+// stream through four 64-row slots.
 //
 // Warp roles (192 threads): 0 = TMA producer, 1 = MMA issuer, 2-5 = the
 // thread-per-row warpgroup (a warp reaches TMEM lanes 32 (warp mod 4) and up).
@@ -44,21 +52,34 @@ namespace {
 
 constexpr int kThreadsB = 192;
 constexpr uint32_t kTmemColsB = 512;
-constexpr int kT = kBwdTcTile;  // keys per CTA, query rows per step
+constexpr int kT = kBwdTcTile;  // keys per dk/dv CTA, query rows per dq CTA
+constexpr int kSub = 64;        // rows of a streamed sub-tile: query rows (dk/dv) or keys (dq) per sub-step
+constexpr int kSlots = 4;       // streamed sub-tile slots in shared memory
 constexpr float kLog2eB = 1.4426950408889634f;
+
+// K-major operand of 128 rows: 16-element K steps within a 64-column box,
+// then the next box (boxes of 128 rows x 128 bytes)
+__device__ __forceinline__ uint32_t kstep128(int kk) {
+  return static_cast<uint32_t>(((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4);
+}
+// the same for a 64-row sub-tile (boxes of 64 rows x 128 bytes)
+__device__ __forceinline__ uint32_t kstep64(int kk) {
+  return static_cast<uint32_t>(((kk >> 2) * (kSub * 128) + (kk & 3) * 32) >> 4);
+}
 
 template <int D>
 struct BSmem {
-  static constexpr int kTile = kT * D * 2;   // one bf16 128-row tile
-  static constexpr int kHalf = kT * 128;     // one 64-column (128-byte) box of a 128-row tile
+  static constexpr int kTile = kT * D * 2;    // one bf16 128-row tile (K or V)
+  static constexpr int kSubT = kSub * D * 2;  // one bf16 64-row sub-tile (Q or dO)
+  static constexpr int kHalfS = kSub * 128;   // one 64-column box of a sub-tile
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTile;
-  static constexpr int kOffQ = kOffV + kTile;      // two slots
-  static constexpr int kOffO = kOffQ + 2 * kTile;  // dO, two slots
-  static constexpr int kOffLse = kOffO + 2 * kTile;   // two slots of 128 floats: lse * log2 e
-  static constexpr int kOffDlt = kOffLse + 2 * kT * 4; // two slots of 128 floats: delta
-  static constexpr int kOffBar = kOffDlt + 2 * kT * 4;
-  static constexpr int kNumBars = 9;
+  static constexpr int kOffQ = kOffV + kTile;            // kSlots sub-tiles
+  static constexpr int kOffO = kOffQ + kSlots * kSubT;   // dO, kSlots sub-tiles
+  static constexpr int kOffLse = kOffO + kSlots * kSubT;     // kSlots x 64 floats: lse * log2 e
+  static constexpr int kOffDlt = kOffLse + kSlots * kSub * 4; // kSlots x 64 floats: delta
+  static constexpr int kOffBar = kOffDlt + kSlots * kSub * 4;
+  static constexpr int kNumBars = 15;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   // + room to align the base to 1024 bytes, as much as the 227 KB budget leaves
@@ -68,17 +89,18 @@ struct BSmem {
 
 enum : int {
   kBarKV = 0,      // K and V tiles landed
-  kBarQFull = 1,   // +slot: Q, dO, lse, delta of a query tile landed (TMA bytes + one arrive)
-  kBarQEmpty = 3,  // +slot: MMAs of the tile done with the slot
-  kBarSFull = 5,   // S^T and dP^T in TMEM
-  kBarPFull = 6,   // P^T, dS^T written (4 softmax warps arrive)
-  kBarDone = 7,    // every MMA of the CTA done: dK, dV final
-  kBarDrain = 8,
+  kBarQFull = 1,   // +slot (4): Q, dO, lse, delta of a sub-tile landed (TMA bytes)
+  kBarQEmpty = 5,  // +slot (4): MMAs done with the slot
+  kBarSFull = 9,   // +TMEM slot (2): S^T and dP^T of the sub-step in TMEM
+  kBarPFull = 11,  // +TMEM slot (2): P^T, dS^T written (4 row warps arrive)
+  kBarDone = 13,   // every MMA of the CTA done: dK, dV final
+  kBarDrain = 14,
 };
 
-// Query tiles of the lap of K/V block jb, in the order the block visits the ranks.
+// 64-row query sub-tiles of the lap of K/V block jb, in the order the block
+// visits the ranks.
 struct QCursor {
-  int t, tile, ntile, off, len;
+  int t, r, tile, ntile, off, len;
   __device__ __forceinline__ void init(const BwdArgs& a, int jb) {
     t = -1;
     next_block(a, jb);
@@ -88,15 +110,15 @@ struct QCursor {
     while (true) {
       ++t;
       if (t >= a.n) return;
-      const int r = (jb + t) % a.n;
+      r = (jb + t) % a.n;
       off = a.off[r];
       len = a.len[r];
-      ntile = (len + kT - 1) / kT;
+      ntile = (len + kSub - 1) / kSub;
       if (ntile > 0) return;
     }
   }
-  __device__ __forceinline__ int q0() const { return off + tile * kT; }
-  __device__ __forceinline__ int nvalid() const { return min(kT, len - tile * kT); }
+  __device__ __forceinline__ int q0() const { return off + tile * kSub; }
+  __device__ __forceinline__ int nvalid() const { return min(kSub, len - tile * kSub); }
   __device__ __forceinline__ void advance(const BwdArgs& a, int jb) {
     if (++tile >= ntile) next_block(a, jb);
   }
@@ -110,11 +132,12 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity, uint
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
+// tq64, to64: Q and dO with 64-row boxes; tk, tv: K and V with 128-row boxes
 template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1)
-    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
-                       const __grid_constant__ BwdArgs a) {
+    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tq64, const __grid_constant__ CUtensorMap tk,
+                            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to64,
+                            const __grid_constant__ BwdArgs a) {
   using L = BSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the swizzled tiles need a 1024-byte aligned base; a base that would need
@@ -141,14 +164,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   while (jb + 1 < a.n && a.kv_prefix[jb + 1] <= static_cast<int>(blockIdx.x)) ++jb;
   const int key0 = a.off[jb] + (static_cast<int>(blockIdx.x) - a.kv_prefix[jb]) * kT;
   const int nk = min(kT, a.off[jb] + a.len[jb] - key0);
-  int NQT = 0;
-  for (int t = 0; t < a.n; ++t) NQT += (a.len[(jb + t) % a.n] + kT - 1) / kT;
+  int NJ = 0;  // 64-row query sub-steps of the lap
+  for (int t = 0; t < a.n; ++t) NJ += (a.len[(jb + t) % a.n] + kSub - 1) / kSub;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
-      const bool two = i == kBarQFull || i == kBarQFull + 1;
-      const bool four = i == kBarPFull;
-      mbar_init(bar(i), two ? 2 : (four ? 4 : 1));
+      const bool four = i == kBarPFull || i == kBarPFull + 1;
+      mbar_init(bar(i), four ? 4 : 1);
     }
     misc[1] = 0;
     fence_mbar_init();
@@ -167,66 +189,58 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     // ===================== TMA producer =====================
     const bool leader = elect_one();
     if (leader) {
-      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tq64);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      tma_prefetch_desc(&to);
+      tma_prefetch_desc(&to64);
       mbar_arrive_expect_tx(bar(kBarKV), 2 * L::kTile);
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_4d(sb + L::kOffK + c * L::kHalf, &tk, bar(kBarKV), c * 64, h, key0, b);
-        tma_load_4d(sb + L::kOffV + c * L::kHalf, &tv, bar(kBarKV), c * 64, h, key0, b);
+        tma_load_4d(sb + L::kOffK + c * (kT * 128), &tk, bar(kBarKV), c * 64, h, key0, b);
+        tma_load_4d(sb + L::kOffV + c * (kT * 128), &tv, bar(kBarKV), c * 64, h, key0, b);
       }
     }
-    int issued[2] = {0, 0};
+    int issued[kSlots] = {0, 0, 0, 0};
     QCursor cur;
     cur.init(a, jb);
-    for (int it = 0; it < NQT; ++it) {
-      const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
+    for (int j = 0; j < NJ; ++j) {
+      const int s = j & (kSlots - 1);
+      const uint32_t ph = (j >> 2) & 1;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarQEmpty + s), ph ^ 1, abort_flag, a.err, tmo))) break;
-      const int q0 = cur.q0(), nq = cur.nvalid();
+      const int q0 = cur.q0();
       if (leader) {
-        mbar_arrive_expect_tx(bar(kBarQFull + s), 2 * L::kTile);
+        mbar_arrive_expect_tx(bar(kBarQFull + s), 2 * L::kSubT + 2 * kSub * 4);
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(sb + L::kOffQ + s * L::kTile + c * L::kHalf, &tq, bar(kBarQFull + s), c * 64, h, q0, b);
-          tma_load_4d(sb + L::kOffO + s * L::kTile + c * L::kHalf, &to, bar(kBarQFull + s), c * 64, h, q0, b);
+          tma_load_4d(sb + L::kOffQ + s * L::kSubT + c * L::kHalfS, &tq64, bar(kBarQFull + s), c * 64, h, q0, b);
+          tma_load_4d(sb + L::kOffO + s * L::kSubT + c * L::kHalfS, &to64, bar(kBarQFull + s), c * 64, h, q0, b);
         }
-      }
-      // the rows' lse (times log2 e) and delta; rows past the tile, and rows
-      // that saw no key, get lse = +inf so that p = 0
-      for (int i = lane; i < kT; i += 32) {
-        float l = INFINITY, dl = 0.f;
-        if (i < nq) {
-          const int64_t o = b * a.l_bstride + static_cast<int64_t>(h) * a.S + q0 + i;
-          l = a.lse[o];
-          l = l == -INFINITY ? INFINITY : l * kLog2eB;
-          dl = a.delta[o];
-        }
-        s_lse[s * kT + i] = l;
-        s_dlt[s * kT + i] = dl;
+        // the rows' lse (times log2 e) and delta from the padded per-shard
+        // copies: rows past the shard, and rows that saw no key, hold lse =
+        // +inf, so that p = 0
+        const int64_t pr = ((static_cast<int64_t>(b) * a.H + h) * a.n + cur.r) * a.lpad + cur.tile * kSub;
+        bulk_g2s(smem_addr(s_lse + s * kSub), a.lse2p + pr, kSub * 4, bar(kBarQFull + s));
+        bulk_g2s(smem_addr(s_dlt + s * kSub), a.dltp + pr, kSub * 4, bar(kBarQFull + s));
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarQFull + s));
       ++issued[s];
       cur.advance(a, jb);
     }
     if (*abort_flag) {
       // let every issued copy land before the CTA's shared memory goes away
       drain_wait_b(bar(kBarKV), 0, tmo);
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < kSlots; ++s)
         if (issued[s]) drain_wait_b(bar(kBarQFull + s), (issued[s] - 1) & 1, tmo);
     }
   } else if (warp == 1) {
     // ===================== MMA issuer =====================
     const bool leader = elect_one();
-    constexpr uint32_t idesc_s = idesc_bf16_f32(kT, kT, false, false);  // S^T, dP^T: M = keys, N = queries
-    constexpr uint32_t idesc_g = idesc_bf16_f32(kT, D, false, true);    // dV, dK: A in TMEM, B MN-major
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kT, kSub, false, false);  // S^T, dP^T: M = keys, N = 64 queries
+    constexpr uint32_t idesc_g = idesc_bf16_f32(kT, D, false, true);      // dV, dK: A in TMEM, B MN-major
     const uint64_t k_km = smem_desc_sw128(sb + L::kOffK, 16, 1024);
     const uint64_t v_km = smem_desc_sw128(sb + L::kOffV, 16, 1024);
     const uint64_t q_km = smem_desc_sw128(sb + L::kOffQ, 16, 1024);
     const uint64_t o_km = smem_desc_sw128(sb + L::kOffO, 16, 1024);
-    const uint64_t q_mn = smem_desc_sw128(sb + L::kOffQ, L::kHalf, 1024);
-    const uint64_t o_mn = smem_desc_sw128(sb + L::kOffO, L::kHalf, 1024);
+    const uint64_t q_mn = smem_desc_sw128(sb + L::kOffQ, L::kHalfS, 1024);
+    const uint64_t o_mn = smem_desc_sw128(sb + L::kOffO, L::kHalfS, 1024);
     const uint32_t km_hi = static_cast<uint32_t>(k_km >> 32), mn_hi = static_cast<uint32_t>(q_mn >> 32);
     const uint32_t k_km_lo = static_cast<uint32_t>(k_km), v_km_lo = static_cast<uint32_t>(v_km);
     const uint32_t q_km_lo = static_cast<uint32_t>(q_km), o_km_lo = static_cast<uint32_t>(o_km);
@@ -234,43 +248,69 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     auto commit = [&](uint32_t bar_addr) {
       if (leader) mma_commit(bar_addr);
     };
-    // K-major operands: 16-element K steps within a 64-column box, then the next box
-    auto kstep = [](int kk) -> uint32_t { return static_cast<uint32_t>(((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4); };
-    bool ok = mbar_wait_bounded(bar(kBarKV), 0, abort_flag, a.err, tmo);
-    for (int it = 0; ok && it < NQT; ++it) {
-      const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      const uint32_t slot = static_cast<uint32_t>((s * L::kTile) >> 4);
-      if (!mbar_wait_bounded(bar(kBarQFull + s), ph, abort_flag, a.err, tmo)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // 1. S^T = K Q^T
+    // S^T and dP^T of the sub-tile in smem slot q, into TMEM slot ts
+    auto issue_sdp = [&](int q, int ts) {
+      const uint32_t slot = static_cast<uint32_t>((q * L::kSubT) >> 4);
+      const uint32_t d = tmem + ts * 128;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        if (leader) mma_ss_lohi(tmem, k_km_lo + kstep(kk), km_hi, q_km_lo + slot + kstep(kk), km_hi, idesc_s, kk > 0);
-      // 2. dP^T = V dO^T
+        if (leader) mma_ss_lohi(d, k_km_lo + kstep128(kk), km_hi, q_km_lo + slot + kstep64(kk), km_hi, idesc_s, kk > 0);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         if (leader)
-          mma_ss_lohi(tmem + 128, v_km_lo + kstep(kk), km_hi, o_km_lo + slot + kstep(kk), km_hi, idesc_s, kk > 0);
-      commit(bar(kBarSFull));
-      if (!mbar_wait_bounded(bar(kBarPFull), it & 1, abort_flag, a.err, tmo)) {
+          mma_ss_lohi(d + kSub, v_km_lo + kstep128(kk), km_hi, o_km_lo + slot + kstep64(kk), km_hi, idesc_s, kk > 0);
+    };
+    // dV += P^T dO and dK += dS^T Q over the sub-tile's 64 query rows (K = rows:
+    // 16 rows = 2048 bytes of an MN-major sub-tile)
+    auto issue_g = [&](int q, int ts, bool acc) {
+      const uint32_t slot = static_cast<uint32_t>((q * L::kSubT) >> 4);
+      const uint32_t pa = tmem + ts * 128;
+#pragma unroll
+      for (int kk = 0; kk < kSub / 16; ++kk)
+        if (leader) mma_ts_lohi(tmem + 256, pa + kk * 8, o_mn_lo + slot + ((kk * 2048) >> 4), mn_hi, idesc_g,
+                                (acc || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < kSub / 16; ++kk)
+        if (leader) mma_ts_lohi(tmem + 256 + D, pa + kSub + kk * 8, q_mn_lo + slot + ((kk * 2048) >> 4), mn_hi,
+                                idesc_g, (acc || kk > 0) ? 1u : 0u);
+    };
+    auto wait_q = [&](int j) -> bool {
+      return mbar_wait_bounded(bar(kBarQFull + (j & (kSlots - 1))), (j >> 2) & 1, abort_flag, a.err, tmo);
+    };
+    bool ok = mbar_wait_bounded(bar(kBarKV), 0, abort_flag, a.err, tmo);
+    // prologue: S^T, dP^T of the first two sub-steps
+    for (int j = 0; ok && j < 2 && j < NJ; ++j) {
+      if (!wait_q(j)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // 3. dV += P^T dO;  4. dK += dS^T Q   (K = query rows: 16 rows = 2048 bytes of an MN-major tile)
-#pragma unroll
-      for (int kk = 0; kk < kT / 16; ++kk)
-        if (leader) mma_ts_lohi(tmem + 256, tmem + kk * 8, o_mn_lo + slot + ((kk * 2048) >> 4), mn_hi, idesc_g,
-                                (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < kT / 16; ++kk)
-        if (leader) mma_ts_lohi(tmem + 256 + D, tmem + 128 + kk * 8, q_mn_lo + slot + ((kk * 2048) >> 4), mn_hi,
-                                idesc_g, (it > 0 || kk > 0) ? 1u : 0u);
-      commit(bar(kBarQEmpty + s));
+      issue_sdp(j, j);
+      commit(bar(kBarSFull + j));
+    }
+    // sub-step j: once P^T, dS^T are in TMEM slot j mod 2, dV and dK consume
+    // them and S^T, dP^T of sub-step j + 2 go into the same slot; the step is
+    // instantiated per smem slot so every operand offset is a constant
+    auto step = [&](auto q_c, int j) -> bool {
+      constexpr int q = decltype(q_c)::value;
+      constexpr int ts = q & 1;
+      if (!mbar_wait_bounded(bar(kBarPFull + ts), (j >> 1) & 1, abort_flag, a.err, tmo)) return false;
+      tc_fence_after();
+      issue_g(q, ts, j > 0);
+      commit(bar(kBarQEmpty + q));
+      if (j + 2 < NJ) {
+        if (!wait_q(j + 2)) return false;
+        tc_fence_after();
+        issue_sdp((q + 2) & (kSlots - 1), ts);
+        commit(bar(kBarSFull + ts));
+      }
+      return true;
+    };
+    for (int j = 0; ok && j < NJ; j += kSlots) {
+      ok = step(std::integral_constant<int, 0>{}, j);
+      if (ok && j + 1 < NJ) ok = step(std::integral_constant<int, 1>{}, j + 1);
+      if (ok && j + 2 < NJ) ok = step(std::integral_constant<int, 2>{}, j + 2);
+      if (ok && j + 3 < NJ) ok = step(std::integral_constant<int, 3>{}, j + 3);
     }
     if (ok) {
       commit(bar(kBarDone));
@@ -279,32 +319,32 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       drain_wait_b(bar(kBarDrain), 0, tmo);
     }
   } else {
-    // ===================== softmax: one thread per key row =====================
+    // ===================== row pass: one thread per key row =====================
     const int wq = warp & 3;
     const int key = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
     const bool kvalid = key < nk;
     const float c2 = a.scale * kLog2eB;
     bool ok = true;
-    for (int it = 0; it < NQT; ++it) {
-      const int s = it & 1;
+    for (int j = 0; j < NJ; ++j) {
+      const int q = j & (kSlots - 1), ts = j & 1;
       ok = __all_sync(0xffffffffu,
-                      mbar_wait_bounded(bar(kBarQFull + s), (it >> 1) & 1, abort_flag, a.err, tmo) &&
-                          mbar_wait_bounded(bar(kBarSFull), it & 1, abort_flag, a.err, tmo));
+                      mbar_wait_bounded(bar(kBarQFull + q), (j >> 2) & 1, abort_flag, a.err, tmo) &&
+                          mbar_wait_bounded(bar(kBarSFull + ts), (j >> 1) & 1, abort_flag, a.err, tmo));
       if (!ok) break;
       tc_fence_after();
-      const float* lse2 = s_lse + s * kT;
-      const float* dlt = s_dlt + s * kT;
+      const uint32_t t_s = tmem + lane_off + ts * 128, t_dp = t_s + kSub;
+      const float* lse2 = s_lse + q * kSub;
+      const float* dlt = s_dlt + q * kSub;
 #pragma unroll 1
-      for (int c = 0; c < kT / 32; ++c) {
+      for (int c = 0; c < kSub / 32; ++c) {
         uint32_t sr[32], dr[32];
         tmem_ld32(t_s + c * 32, sr);
         tmem_ld32(t_dp + c * 32, dr);
         tmem_wait_ld();
         uint32_t pp[16], dd[16];
         if (kvalid) {
-          // p = 2^(s c2 - lse2) (lse2 = +inf past the tile: p = 0), ds = p (dp - delta); pairs of
+          // p = 2^(s c2 - lse2) (lse2 = +inf past the sub-tile: p = 0), ds = p (dp - delta); pairs of
           // columns in packed fp32x2 FMAs, lse and delta read as 16-byte vectors
           const float4* l4 = reinterpret_cast<const float4*>(lse2 + c * 32);
           const float4* d4 = reinterpret_cast<const float4*>(dlt + c * 32);
@@ -335,7 +375,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPFull));
+      if (lane == 0) mbar_arrive(bar(kBarPFull + ts));
     }
     // ---- dk, dv of this CTA's keys ----
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarDone), 0, abort_flag, a.err, tmo));
@@ -374,28 +414,28 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
 // ----------------------------------------------------------------------------
 // dq: one CTA per 128 query rows of one (batch entry, head); Q and dO loaded
-// once, K and V tiles of the rank's lap streamed in ring order ((r - t) mod n)
-// through two stages. Per K/V tile three MMAs (M = 128 query rows):
-//   S  = Q K^T    (SS, both K-major)                     -> TMEM [0, 128) or [384, 512)
-//   dP = dO V^T   (SS)                                   -> TMEM [128, 256)
-//   dQ += dS K    (TS: dS in TMEM over S's consumed columns, K read MN-major)
-//                                                        -> TMEM [256, 256 + D)
-// S alternates between its two slots, so the next tile's S is computed while
-// the row pass works on this tile; dP, read by the same pass, has one slot.
-// Warps 2-5 (one thread per query row, lse and delta in registers) form
-// dS = p (dp - delta) between the first two and the third. dq is stored once,
+// once, 64-key K and V sub-tiles of the rank's lap streamed in ring order
+// ((r - t) mod n) through four slots. Per sub-tile three MMAs (M = 128 rows):
+//   S  = Q K^T    (SS, both K-major; N = 64)    -> TMEM slot j mod 2, [0, 64)
+//   dP = dO V^T   (SS)                          -> the same slot, [64, 128)
+//   dQ += dS K    (TS: dS over S's first 32 columns, K read MN-major)
+//                                               -> TMEM [256, 256 + D)
+// S and dP of sub-step j + 2 are issued right after dQ of sub-step j, so
+// they run while warps 2-5 (one thread per query row, lse and delta in
+// registers) form dS = p (dp - delta) of sub-step j + 1. dq is stored once,
 // without atomics.
 // ----------------------------------------------------------------------------
 template <int D>
 struct DqSmem {
-  static constexpr int kTile = kT * D * 2;
-  static constexpr int kHalf = kT * 128;
+  static constexpr int kTile = kT * D * 2;    // Q or dO: 128 rows
+  static constexpr int kSubT = kSub * D * 2;  // a K or V sub-tile: 64 keys
+  static constexpr int kHalfS = kSub * 128;
   static constexpr int kOffQ = 0;
   static constexpr int kOffO = kTile;
-  static constexpr int kOffK = 2 * kTile;  // two stages
-  static constexpr int kOffV = 4 * kTile;  // two stages
-  static constexpr int kOffBar = 6 * kTile;
-  static constexpr int kNumBars = 9;
+  static constexpr int kOffK = 2 * kTile;                 // kSlots sub-tiles
+  static constexpr int kOffV = kOffK + kSlots * kSubT;    // kSlots sub-tiles
+  static constexpr int kOffBar = kOffV + kSlots * kSubT;
+  static constexpr int kNumBars = 14;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kMax = 227 * 1024;
@@ -404,15 +444,15 @@ struct DqSmem {
 
 enum : int {
   kDqBarQ = 0,        // Q and dO landed
-  kDqBarKVFull = 1,   // +stage: K and V tiles landed
-  kDqBarKVEmpty = 3,  // +stage: MMAs done with the stage
-  kDqBarSFull = 5,    // S and dP in TMEM
-  kDqBarPFull = 6,    // dS written (4 softmax warps arrive)
-  kDqBarDone = 7,     // every MMA done: dQ final
-  kDqBarDrain = 8,
+  kDqBarKVFull = 1,   // +slot (4): K and V sub-tiles landed
+  kDqBarKVEmpty = 5,  // +slot (4): MMAs done with the slot
+  kDqBarSFull = 9,    // +TMEM slot (2): S and dP in TMEM
+  kDqBarPFull = 11,   // +TMEM slot (2): dS written (4 row warps arrive)
+  kDqBarDone = 13,    // every MMA done: dQ final
+  kDqBarDrain = 14,
 };
 
-// K/V tiles of rank r's lap, blocks in ring order (r - t) mod n.
+// 64-key K/V sub-tiles of rank r's lap, blocks in ring order (r - t) mod n.
 struct KvWalk {
   int t, tile, ntile, off, len;
   __device__ __forceinline__ void init(const BwdArgs& a, int r) {
@@ -428,21 +468,22 @@ struct KvWalk {
       if (j < 0) j += a.n;
       off = a.off[j];
       len = a.len[j];
-      ntile = (len + kT - 1) / kT;
+      ntile = (len + kSub - 1) / kSub;
       if (ntile > 0) return;
     }
   }
-  __device__ __forceinline__ int k0() const { return off + tile * kT; }
-  __device__ __forceinline__ int nvalid() const { return min(kT, len - tile * kT); }
+  __device__ __forceinline__ int k0() const { return off + tile * kSub; }
+  __device__ __forceinline__ int nvalid() const { return min(kSub, len - tile * kSub); }
   __device__ __forceinline__ void advance(const BwdArgs& a, int r) {
     if (++tile >= ntile) next_block(a, r);
   }
 };
 
+// tq, to: Q and dO with 128-row boxes; tk64, tv64: K and V with 64-row boxes
 template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1)
-    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                          const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk64,
+                          const __grid_constant__ CUtensorMap tv64, const __grid_constant__ CUtensorMap to,
                           const __grid_constant__ BwdArgs a) {
   using L = DqSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -465,15 +506,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   while (r + 1 < a.n && a.q_prefix[r + 1] <= static_cast<int>(blockIdx.x)) ++r;
   const int q0 = a.off[r] + (static_cast<int>(blockIdx.x) - a.q_prefix[r]) * kT;
   const int nq = min(kT, a.off[r] + a.len[r] - q0);
-  int NT = 0;
+  int NJ = 0;  // 64-key sub-steps of the lap
   for (int t = 0; t < a.n; ++t) {
     int j = (r - t) % a.n;
     if (j < 0) j += a.n;
-    NT += (a.len[j] + kT - 1) / kT;
+    NJ += (a.len[j] + kSub - 1) / kSub;
   }
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), i == kDqBarPFull ? 4 : 1);
+    for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), (i == kDqBarPFull || i == kDqBarPFull + 1) ? 4 : 1);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -492,30 +533,30 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const bool leader = elect_one();
     if (leader) {
       tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&tk64);
+      tma_prefetch_desc(&tv64);
       tma_prefetch_desc(&to);
       mbar_arrive_expect_tx(bar(kDqBarQ), 2 * L::kTile);
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_4d(sb + L::kOffQ + c * L::kHalf, &tq, bar(kDqBarQ), c * 64, h, q0, b);
-        tma_load_4d(sb + L::kOffO + c * L::kHalf, &to, bar(kDqBarQ), c * 64, h, q0, b);
+        tma_load_4d(sb + L::kOffQ + c * (kT * 128), &tq, bar(kDqBarQ), c * 64, h, q0, b);
+        tma_load_4d(sb + L::kOffO + c * (kT * 128), &to, bar(kDqBarQ), c * 64, h, q0, b);
       }
     }
-    int issued[2] = {0, 0};
+    int issued[kSlots] = {0, 0, 0, 0};
     KvWalk cur;
     cur.init(a, r);
-    for (int it = 0; it < NT; ++it) {
-      const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
+    for (int j = 0; j < NJ; ++j) {
+      const int s = j & (kSlots - 1);
+      const uint32_t ph = (j >> 2) & 1;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kDqBarKVEmpty + s), ph ^ 1, abort_flag, a.err, tmo)))
         break;
       if (leader) {
-        mbar_arrive_expect_tx(bar(kDqBarKVFull + s), 2 * L::kTile);
+        mbar_arrive_expect_tx(bar(kDqBarKVFull + s), 2 * L::kSubT);
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(sb + L::kOffK + s * L::kTile + c * L::kHalf, &tk, bar(kDqBarKVFull + s), c * 64, h, cur.k0(),
-                      b);
-          tma_load_4d(sb + L::kOffV + s * L::kTile + c * L::kHalf, &tv, bar(kDqBarKVFull + s), c * 64, h, cur.k0(),
-                      b);
+          tma_load_4d(sb + L::kOffK + s * L::kSubT + c * L::kHalfS, &tk64, bar(kDqBarKVFull + s), c * 64, h,
+                      cur.k0(), b);
+          tma_load_4d(sb + L::kOffV + s * L::kSubT + c * L::kHalfS, &tv64, bar(kDqBarKVFull + s), c * 64, h,
+                      cur.k0(), b);
         }
       }
       ++issued[s];
@@ -524,19 +565,19 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     if (*abort_flag) {
       // let every issued copy land before the CTA's shared memory goes away
       drain_wait_b(bar(kDqBarQ), 0, tmo);
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < kSlots; ++s)
         if (issued[s]) drain_wait_b(bar(kDqBarKVFull + s), (issued[s] - 1) & 1, tmo);
     }
   } else if (warp == 1) {
     // ===================== MMA issuer =====================
     const bool leader = elect_one();
-    constexpr uint32_t idesc_s = idesc_bf16_f32(kT, kT, false, false);  // S, dP: M = query rows, N = keys
-    constexpr uint32_t idesc_q = idesc_bf16_f32(kT, D, false, true);    // dQ: A (dS) in TMEM, B (K) MN-major
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kT, kSub, false, false);  // S, dP: M = query rows, N = 64 keys
+    constexpr uint32_t idesc_q = idesc_bf16_f32(kT, D, false, true);      // dQ: A (dS) in TMEM, B (K) MN-major
     const uint64_t q_km = smem_desc_sw128(sb + L::kOffQ, 16, 1024);
     const uint64_t o_km = smem_desc_sw128(sb + L::kOffO, 16, 1024);
     const uint64_t k_km = smem_desc_sw128(sb + L::kOffK, 16, 1024);
     const uint64_t v_km = smem_desc_sw128(sb + L::kOffV, 16, 1024);
-    const uint64_t k_mn = smem_desc_sw128(sb + L::kOffK, L::kHalf, 1024);
+    const uint64_t k_mn = smem_desc_sw128(sb + L::kOffK, L::kHalfS, 1024);
     const uint32_t km_hi = static_cast<uint32_t>(q_km >> 32), mn_hi = static_cast<uint32_t>(k_mn >> 32);
     const uint32_t q_lo = static_cast<uint32_t>(q_km), o_lo = static_cast<uint32_t>(o_km);
     const uint32_t k_lo = static_cast<uint32_t>(k_km), v_lo = static_cast<uint32_t>(v_km);
@@ -544,61 +585,57 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     auto commit = [&](uint32_t bar_addr) {
       if (leader) mma_commit(bar_addr);
     };
-    auto kstep = [](int kk) -> uint32_t { return static_cast<uint32_t>(((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4); };
-    // S of tile it lives in TMEM [0, 128) for even it, [384, 512) for odd it, so
-    // the next tile's S = Q K^T runs while the row pass works on this tile's
-    auto wait_kv = [&](int it) -> bool {
-      return mbar_wait_bounded(bar(kDqBarKVFull + (it & 1)), (it >> 1) & 1, abort_flag, a.err, tmo);
-    };
-    auto issue_s = [&](int it) {
-      const uint32_t stage = static_cast<uint32_t>(((it & 1) * L::kTile) >> 4);
-      const uint32_t d_tmem = tmem + ((it & 1) ? 384u : 0u);
+    // S and dP of the K/V sub-tile in smem slot q, into TMEM slot ts
+    auto issue_sdp = [&](int q, int ts) {
+      const uint32_t slot = static_cast<uint32_t>((q * L::kSubT) >> 4);
+      const uint32_t d = tmem + ts * 128;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        if (leader) mma_ss_lohi(d_tmem, q_lo + kstep(kk), km_hi, k_lo + stage + kstep(kk), km_hi, idesc_s, kk > 0);
-    };
-    auto issue_dp = [&](int it) {
-      const uint32_t stage = static_cast<uint32_t>(((it & 1) * L::kTile) >> 4);
+        if (leader) mma_ss_lohi(d, q_lo + kstep128(kk), km_hi, k_lo + slot + kstep64(kk), km_hi, idesc_s, kk > 0);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        if (leader) mma_ss_lohi(tmem + 128, o_lo + kstep(kk), km_hi, v_lo + stage + kstep(kk), km_hi, idesc_s, kk > 0);
+        if (leader) mma_ss_lohi(d + kSub, o_lo + kstep128(kk), km_hi, v_lo + slot + kstep64(kk), km_hi, idesc_s, kk > 0);
     };
-    bool ok = mbar_wait_bounded(bar(kDqBarQ), 0, abort_flag, a.err, tmo) && (NT == 0 || wait_kv(0));
-    if (ok && NT > 0) {
-      tc_fence_after();
-      issue_s(0);
-      issue_dp(0);
-      commit(bar(kDqBarSFull));
-    }
-    for (int it = 0; ok && it < NT; ++it) {
-      const int s = it & 1;
-      const uint32_t stage = static_cast<uint32_t>((s * L::kTile) >> 4);
-      // the next tile's S: its slot's last reader (dQ of tile it - 1) is already issued
-      if (it + 1 < NT) {
-        if (!wait_kv(it + 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_s(it + 1);
-      }
-      if (!mbar_wait_bounded(bar(kDqBarPFull), it & 1, abort_flag, a.err, tmo)) {
+    auto wait_kv = [&](int j) -> bool {
+      return mbar_wait_bounded(bar(kDqBarKVFull + (j & (kSlots - 1))), (j >> 2) & 1, abort_flag, a.err, tmo);
+    };
+    bool ok = mbar_wait_bounded(bar(kDqBarQ), 0, abort_flag, a.err, tmo);
+    for (int j = 0; ok && j < 2 && j < NJ; ++j) {
+      if (!wait_kv(j)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // dQ += dS K   (dS over S's first 64 columns; K = keys: 16 key rows = 2048 bytes of the MN-major K tile)
-      const uint32_t a_tmem = tmem + (s ? 384u : 0u);
+      issue_sdp(j, j);
+      commit(bar(kDqBarSFull + j));
+    }
+    // sub-step j: dQ += dS K once dS is in TMEM slot j mod 2 (K = keys: 16 key
+    // rows = 2048 bytes of the MN-major sub-tile), then S, dP of sub-step j + 2
+    // into the same slot; instantiated per smem slot
+    auto step = [&](auto q_c, int j) -> bool {
+      constexpr int q = decltype(q_c)::value;
+      constexpr int ts = q & 1;
+      if (!mbar_wait_bounded(bar(kDqBarPFull + ts), (j >> 1) & 1, abort_flag, a.err, tmo)) return false;
+      tc_fence_after();
+      const uint32_t slot = static_cast<uint32_t>((q * L::kSubT) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < kT / 16; ++kk)
-        if (leader) mma_ts_lohi(tmem + 256, a_tmem + kk * 8, k_mn_lo + stage + ((kk * 2048) >> 4), mn_hi, idesc_q,
-                                (it > 0 || kk > 0) ? 1u : 0u);
-      commit(bar(kDqBarKVEmpty + s));
-      // the next tile's dP, now that the row pass has read this one
-      if (it + 1 < NT) {
-        issue_dp(it + 1);
-        commit(bar(kDqBarSFull));
+      for (int kk = 0; kk < kSub / 16; ++kk)
+        if (leader) mma_ts_lohi(tmem + 256, tmem + ts * 128 + kk * 8, k_mn_lo + slot + ((kk * 2048) >> 4), mn_hi,
+                                idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
+      commit(bar(kDqBarKVEmpty + q));
+      if (j + 2 < NJ) {
+        if (!wait_kv(j + 2)) return false;
+        tc_fence_after();
+        issue_sdp((q + 2) & (kSlots - 1), ts);
+        commit(bar(kDqBarSFull + ts));
       }
+      return true;
+    };
+    for (int j = 0; ok && j < NJ; j += kSlots) {
+      ok = step(std::integral_constant<int, 0>{}, j);
+      if (ok && j + 1 < NJ) ok = step(std::integral_constant<int, 1>{}, j + 1);
+      if (ok && j + 2 < NJ) ok = step(std::integral_constant<int, 2>{}, j + 2);
+      if (ok && j + 3 < NJ) ok = step(std::integral_constant<int, 3>{}, j + 3);
     }
     if (ok) {
       commit(bar(kDqBarDone));
@@ -611,7 +648,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t t_dp = tmem + lane_off + 128;
     const float c2 = a.scale * kLog2eB;
     // the row's lse (times log2 e) and delta; a row past the shard, or one that
     // saw no key, gets lse = +inf so that p = 0
@@ -625,14 +661,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     bool ok = true;
     KvWalk cur;
     cur.init(a, r);
-    for (int it = 0; it < NT; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kDqBarSFull), it & 1, abort_flag, a.err, tmo));
+    for (int j = 0; j < NJ; ++j) {
+      const int ts = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kDqBarSFull + ts), (j >> 1) & 1, abort_flag, a.err, tmo));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t t_s = tmem + lane_off + ((it & 1) ? 384u : 0u);  // this tile's S slot
+      const uint32_t t_s = tmem + lane_off + ts * 128, t_dp = t_s + kSub;  // this sub-step's slot
       const int nvk = cur.nvalid();
 #pragma unroll 1
-      for (int c = 0; c < kT / 32; ++c) {
+      for (int c = 0; c < kSub / 32; ++c) {
         uint32_t sr[32], dr[32];
         tmem_ld32(t_s + c * 32, sr);
         tmem_ld32(t_dp + c * 32, dr);
@@ -645,7 +682,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           fma_f32x2(g0, g1, u2f(dr[e]), u2f(dr[e + 1]), 1.f, ndl);
           const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
           fma2(d0, d1, p0, p1, g0, g1, 0.f, 0.f);
-          // keys past the K/V tile (the next block's rows, or zero fill) take no part
+          // keys past the sub-tile (the next block's rows, or zero fill) take no part
           d0 = c * 32 + e < nvk ? d0 : 0.f;
           d1 = c * 32 + e + 1 < nvk ? d1 : 0.f;
           dd[e >> 1] = pack_bf16x2(d0, d1);
@@ -656,7 +693,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kDqBarPFull));
+      if (lane == 0) mbar_arrive(bar(kDqBarPFull + ts));
       cur.advance(a, r);
     }
     // ---- dq of this CTA's rows ----
@@ -691,8 +728,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 }
 
 template <int D>
-cudaError_t launch_bwd_tc_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& to, cudaStream_t s) {
+cudaError_t launch_bwd_tc_d(const BwdArgs& a, const BwdTensorMaps& m, cudaStream_t s) {
   using L = BSmem<D>;
   using LQ = DqSmem<D>;
   static_assert(L::kAlloc <= 227 * 1024 && LQ::kAlloc <= 227 * 1024, "shared memory budget");
@@ -703,11 +739,12 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, const CUtensorMap& tq, const CUten
   if (e != cudaSuccess) return e;
   if (a.H == 0 || a.B == 0) return cudaSuccess;
   if (a.kv_prefix[a.n] > 0) {
-    attn_bwd_dkdv_tc_kernel<D><<<dim3(a.kv_prefix[a.n], a.H, a.B), kThreadsB, L::kAlloc, s>>>(tq, tk, tv, to, a);
+    attn_bwd_dkdv_tc_kernel<D>
+        <<<dim3(a.kv_prefix[a.n], a.H, a.B), kThreadsB, L::kAlloc, s>>>(m.q64, m.k, m.v, m.o64, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.q_prefix[a.n] > 0) {
-    attn_bwd_dq_tc_kernel<D><<<dim3(a.q_prefix[a.n], a.H, a.B), kThreadsB, LQ::kAlloc, s>>>(tq, tk, tv, to, a);
+    attn_bwd_dq_tc_kernel<D><<<dim3(a.q_prefix[a.n], a.H, a.B), kThreadsB, LQ::kAlloc, s>>>(m.q, m.k64, m.v64, m.o, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -715,10 +752,9 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, const CUtensorMap& tq, const CUten
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_tc(const BwdArgs& a, int D, const CUtensorMap& tq, const CUtensorMap& tk,
-                               const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t s) {
-  if (D == 128) return launch_bwd_tc_d<128>(a, tq, tk, tv, to, s);
-  if (D == 64) return launch_bwd_tc_d<64>(a, tq, tk, tv, to, s);
+cudaError_t launch_attn_bwd_tc(const BwdArgs& a, int D, const BwdTensorMaps& m, cudaStream_t s) {
+  if (D == 128) return launch_bwd_tc_d<128>(a, m, s);
+  if (D == 64) return launch_bwd_tc_d<64>(a, m, s);
   return cudaErrorInvalidValue;
 }
 

@@ -82,14 +82,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // (row = H*D for a dense tensor; larger for a range of its heads); box = 64
 // columns x 128 tokens of one head, 128-byte swizzle (the K-major operand
 // layout the MMA descriptors expect).
-bool make_tmap_bf16(CUtensorMap* m, const void* base, int D, int H, int S, int Bn, int64_t row, int64_t bstride) {
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int D, int H, int S, int Bn, int64_t row, int64_t bstride,
+                    int box_rows = cp::kTileM) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
                         static_cast<cuuint64_t>(Bn)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(row) * 2,
                            static_cast<cuuint64_t>(bstride) * 2};
-  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(cp::kTileM), 1};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -856,12 +857,18 @@ namespace {
 // Workspace layout of cp_attention_bwd (every piece 256-byte aligned):
 // delta [B, H, S]; with Ulysses, the head-group copies of q, k, v, dout
 // [U][B, S, H/U, D], of lse and delta [U][B, H/U, S], and the head-group
-// gradients dq, dk, dv [U][B, S, H/U, D] fp32.
+// gradients dq, dk, dv [U][B, S, H/U, D] fp32; for bf16, the tensor-core
+// dk/dv kernel's per-shard padded lse * log2 e and delta (BwdArgs::lse2p).
 struct BwdWs {
-  size_t delta = 0, qh = 0, kh = 0, vh = 0, doh = 0, lh = 0, dlh = 0, dqh = 0, dkh = 0, dvh = 0, total = 0;
+  size_t delta = 0, qh = 0, kh = 0, vh = 0, doh = 0, lh = 0, dlh = 0, dqh = 0, dkh = 0, dvh = 0, l2p = 0, dlp = 0,
+         total = 0;
+  int lpad = 0;
 };
 
-BwdWs bwd_ws_layout(int B, int H, int S, int D, int U, cp_dtype dt) {
+// rows of a shard in the padded lse / delta layout: the longest shard, rounded up to 64
+int bwd_lpad(int S, int R) { return (S / R + (S % R ? 1 : 0) + 63) / 64 * 64; }
+
+BwdWs bwd_ws_layout(int B, int H, int S, int D, int R, int U, cp_dtype dt) {
   BwdWs w;
   // U head groups of ceil(H/U) heads (the last head of a short group is padding)
   const size_t Hp = U > 1 ? static_cast<size_t>((H + U - 1) / U) * U : static_cast<size_t>(H);
@@ -883,6 +890,12 @@ BwdWs bwd_ws_layout(int B, int H, int S, int D, int U, cp_dtype dt) {
     w.dqh = take(n * 4);
     w.dkh = take(n * 4);
     w.dvh = take(n * 4);
+  }
+  if (dt == CP_BF16 && R >= 1) {
+    w.lpad = bwd_lpad(S, R);
+    const size_t np = static_cast<size_t>(B) * Hp * R * w.lpad;
+    w.l2p = take(np * 4);
+    w.dlp = take(np * 4);
   }
   w.total = o;
   return w;
@@ -958,15 +971,17 @@ extern "C" {
 
 size_t cp_attention_bwd_workspace_size(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt) {
   if (B < 0 || H < 1 || S < 0 || D < 1 || ring_degree < 1 || ulysses_degree < 1) return 0;
-  return bwd_ws_layout(B, H, S, D, ulysses_degree, dt).total;
+  return bwd_ws_layout(B, H, S, D, ring_degree, ulysses_degree, dt).total;
 }
 
 int cp_attention_bwd_launch_count(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt) {
   if (B <= 0 || S <= 0 || H < 1 || D < 1 || ring_degree < 1 || ulysses_degree < 1) return 0;
   const int U = ulysses_degree;
-  int n = 3;  // delta, then the dk/dv and dq kernels (tensor cores for bf16, CUDA cores for fp32)
+  // delta, then the dk/dv and dq kernels (tensor cores for bf16, CUDA cores
+  // for fp32); bf16 adds the padded lse / delta copy of the dk/dv kernel
+  int n = dt == CP_BF16 ? 4 : 3;
   if (U > 1 && U <= H) {
-    const BwdWs w = bwd_ws_layout(B, H, S, D, U, dt);
+    const BwdWs w = bwd_ws_layout(B, H, S, D, ring_degree, U, dt);
     char* base = reinterpret_cast<char*>(uintptr_t{1} << 20);
     const void* src[4] = {base, base, base, base};
     void* dst[4] = {base + w.qh, base + w.kh, base + w.vh, base + w.doh};
@@ -998,7 +1013,7 @@ cp_status cp_attention_bwd(const void* q, const void* k, const void* v, const fl
     if (!aligned16(p)) return CP_ERR_ALIGNMENT;
   }
   const int R = ring_degree, U = ulysses_degree;
-  const BwdWs w = bwd_ws_layout(B, H, S, D, U, dt);
+  const BwdWs w = bwd_ws_layout(B, H, S, D, R, U, dt);
   if (!workspace || ws_bytes < w.total) return CP_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return CP_ERR_ALIGNMENT;
   DeviceInfo* dev = nullptr;
@@ -1023,17 +1038,25 @@ cp_status cp_attention_bwd(const void* q, const void* k, const void* v, const fl
   a.scale = scale;
   a.err = dev->err;
   a.timeout_ns = kWaitTimeoutNs;
+  a.lse2p = reinterpret_cast<float*>(ws + w.l2p);
+  a.dltp = reinterpret_cast<float*>(ws + w.dlp);
+  a.lpad = w.lpad;
   // bf16: tensor maps over the (possibly head-grouped) q, k, v, dout, then the tensor-core kernels
   auto run = [&](int Bn, int Hx) -> cp_status {
     if (!bf16) return cp::launch_attn_bwd(a, D, false, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
-    CUtensorMap tq, tk, tv, to;
+    if (cp::launch_attn_bwd_prep(a, s) != cudaSuccess) return CP_ERR_CUDA;
+    cp::BwdTensorMaps m;
     const int64_t row = static_cast<int64_t>(Hx) * D;
-    if (!make_tmap_bf16(&tq, a.q, D, Hx, S, Bn, row, a.bstride) ||
-        !make_tmap_bf16(&tk, a.k, D, Hx, S, Bn, row, a.bstride) ||
-        !make_tmap_bf16(&tv, a.v, D, Hx, S, Bn, row, a.bstride) ||
-        !make_tmap_bf16(&to, a.dout, D, Hx, S, Bn, row, a.bstride))
+    if (!make_tmap_bf16(&m.q, a.q, D, Hx, S, Bn, row, a.bstride) ||
+        !make_tmap_bf16(&m.k, a.k, D, Hx, S, Bn, row, a.bstride) ||
+        !make_tmap_bf16(&m.v, a.v, D, Hx, S, Bn, row, a.bstride) ||
+        !make_tmap_bf16(&m.o, a.dout, D, Hx, S, Bn, row, a.bstride) ||
+        !make_tmap_bf16(&m.q64, a.q, D, Hx, S, Bn, row, a.bstride, 64) ||
+        !make_tmap_bf16(&m.k64, a.k, D, Hx, S, Bn, row, a.bstride, 64) ||
+        !make_tmap_bf16(&m.v64, a.v, D, Hx, S, Bn, row, a.bstride, 64) ||
+        !make_tmap_bf16(&m.o64, a.dout, D, Hx, S, Bn, row, a.bstride, 64))
       return CP_ERR_CUDA;
-    return cp::launch_attn_bwd_tc(a, D, tq, tk, tv, to, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+    return cp::launch_attn_bwd_tc(a, D, m, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
   };
   if (U == 1) {
     a.B = B;

@@ -111,24 +111,40 @@ struct BwdArgs {
   // hv_bpg = 0: no padding.
   int hv_bpg;
   int hv_short_from;
+  // tensor-core dk/dv kernel: per (batch entry, head, shard) the shard's rows'
+  // lse * log2 e (+inf where lse = -inf) and delta, each shard padded to lpad
+  // rows (a multiple of 64, the padding holding +inf and 0), so that every
+  // 64-row piece starts 256-byte aligned for a bulk copy
+  float* lse2p;
+  float* dltp;
+  int lpad;
 };
 
 __host__ __device__ inline bool bwd_head_is_padding(const BwdArgs& a, int h, int b) {
   return a.hv_bpg > 0 && h == a.H - 1 && b / a.hv_bpg >= a.hv_short_from;
 }
-constexpr int kBwdTcTile = 128;  // tensor-core backward: keys or query rows per CTA and per step
+constexpr int kBwdTcTile = 128;  // tensor-core backward: keys (dk/dv) or query rows (dq) per CTA
 
 // Launchers (each returns the launch error, cudaSuccess if none).
 // dq, then dk/dv, for D in {64, 128}; bf16 or fp32 inputs.
 cudaError_t launch_attn_bwd(const BwdArgs& a, int D, bool bf16, cudaStream_t s);
+// Fills a.lse2p and a.dltp (see BwdArgs) from a.lse and a.delta.
+cudaError_t launch_attn_bwd_prep(const BwdArgs& a, cudaStream_t s);
 // delta[b, h, s] = sum_d out[b, s, h, d] * dout[b, s, h, d] over dense [B, S, H, D].
 cudaError_t launch_attn_bwd_delta(const float* out, const void* dout, float* delta, int B, int S, int H, int D,
                                   bool bf16, cudaStream_t s);
-// Tensor-core backward for bf16 q, k, v, dout with tensor maps of box {64, 1, 128, 1}
-// (128-byte swizzle): the dk/dv kernel (one CTA per 128 keys, kv_prefix) and the
-// dq kernel (one CTA per 128 query rows, q_prefix); dq, dk, dv written.
-cudaError_t launch_attn_bwd_tc(const BwdArgs& a, int D, const CUtensorMap& tq, const CUtensorMap& tk,
-                               const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t s);
+// Tensor maps of the tensor-core backward over bf16 q, k, v, dout (128-byte
+// swizzle, boxes of 64 columns of one head): boxes of 128 rows for the tiles a
+// CTA keeps (K, V in dk/dv; Q, dO in dq) and of 64 rows for the sub-tiles it
+// streams (Q, dO in dk/dv; K, V in dq).
+struct BwdTensorMaps {
+  CUtensorMap q, k, v, o;          // 128-row boxes
+  CUtensorMap q64, k64, v64, o64;  // 64-row boxes
+};
+// Tensor-core backward for bf16: the dk/dv kernel (one CTA per 128 keys,
+// kv_prefix) and the dq kernel (one CTA per 128 query rows, q_prefix); dq,
+// dk, dv written.
+cudaError_t launch_attn_bwd_tc(const BwdArgs& a, int D, const BwdTensorMaps& m, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t s);
 cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t s);
