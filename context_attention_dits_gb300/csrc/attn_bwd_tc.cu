@@ -25,11 +25,11 @@
 // they run while the row pass works on sub-step j + 1. Q, dO, lse and delta
 // stream through four 64-row slots. After the last sub-tile it writes dk, dv.
 //
-// dq: one CTA owns 128 query rows (Q and dO loaded once) and walks the
-// 64-key K/V sub-tiles of its rank's lap in ring order ((r - t) mod n):
-// S = Q K^T and dP = dO V^T (N = 64) into TMEM slot j mod 2, then dQ += dS K
-// with dS (a thread per query row) over S's first 32 columns; dq is stored
-// once. It recomputes S and dP, 1.4x the MMA work of a single fused kernel,
+// dq: one CTA owns 128 query rows, whose Q and dO rows the row warps place
+// in TMEM once, and walks the 64-key K/V sub-tiles of its rank's lap in ring
+// order ((r - t) mod n): S = Q K^T and dP = dO V^T (N = 64, A read from
+// TMEM) into TMEM slot j mod 2, then dQ += dS K with dS (a thread per query
+// row) over S's first 32 columns; dq is stored once. It recomputes S and dP, 1.4x the MMA work of a single fused kernel,
 // in exchange for no reduction of dq tiles across key-tile CTAs. K and V
 // stream through four 64-row slots.
 //
@@ -413,29 +413,30 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 }
 
 // ----------------------------------------------------------------------------
-// dq: one CTA per 128 query rows of one (batch entry, head); Q and dO loaded
-// once, 64-key K and V sub-tiles of the rank's lap streamed in ring order
-// ((r - t) mod n) through four slots. Per sub-tile three MMAs (M = 128 rows):
-//   S  = Q K^T    (SS, both K-major; N = 64)    -> TMEM slot j mod 2, [0, 64)
-//   dP = dO V^T   (SS)                          -> the same slot, [64, 128)
+// dq: one CTA per 128 query rows of one (batch entry, head). The row warps
+// load the CTA's Q and dO rows once into TMEM (bf16 pairs, the A-operand
+// layout: columns [384, 384 + D/2) and [384 + D/2, 384 + D)); 64-key K and V
+// sub-tiles of the rank's lap stream in ring order ((r - t) mod n) through
+// kDqSlots shared-memory slots. Per sub-tile three MMAs (M = 128 rows):
+//   S  = Q K^T    (TS: Q in TMEM, K K-major; N = 64) -> TMEM slot j mod 2, [0, 64)
+//   dP = dO V^T   (TS)                               -> the same slot, [64, 128)
 //   dQ += dS K    (TS: dS over S's first 32 columns, K read MN-major)
-//                                               -> TMEM [256, 256 + D)
-// S and dP of sub-step j + 2 are issued right after dQ of sub-step j, so
-// they run while warps 2-5 (one thread per query row, lse and delta in
-// registers) form dS = p (dp - delta) of sub-step j + 1. dq is stored once,
-// without atomics.
+//                                                    -> TMEM [256, 256 + D)
+// Only K and V come from shared memory. S and dP of sub-step j + 2 are issued
+// right after dQ of sub-step j, so they run while warps 2-5 (one thread per
+// query row, lse and delta in registers) form dS = p (dp - delta) of
+// sub-step j + 1. dq is stored once, without atomics.
 // ----------------------------------------------------------------------------
+constexpr int kDqSlots = 6;  // K/V sub-tile slots of the dq kernel
+
 template <int D>
 struct DqSmem {
-  static constexpr int kTile = kT * D * 2;    // Q or dO: 128 rows
   static constexpr int kSubT = kSub * D * 2;  // a K or V sub-tile: 64 keys
   static constexpr int kHalfS = kSub * 128;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffO = kTile;
-  static constexpr int kOffK = 2 * kTile;                 // kSlots sub-tiles
-  static constexpr int kOffV = kOffK + kSlots * kSubT;    // kSlots sub-tiles
-  static constexpr int kOffBar = kOffV + kSlots * kSubT;
-  static constexpr int kNumBars = 14;
+  static constexpr int kOffK = 0;                          // kDqSlots sub-tiles
+  static constexpr int kOffV = kOffK + kDqSlots * kSubT;   // kDqSlots sub-tiles
+  static constexpr int kOffBar = kOffV + kDqSlots * kSubT;
+  static constexpr int kNumBars = 1 + 2 * kDqSlots + 6;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kMax = 227 * 1024;
@@ -443,13 +444,13 @@ struct DqSmem {
 };
 
 enum : int {
-  kDqBarQ = 0,        // Q and dO landed
-  kDqBarKVFull = 1,   // +slot (4): K and V sub-tiles landed
-  kDqBarKVEmpty = 5,  // +slot (4): MMAs done with the slot
-  kDqBarSFull = 9,    // +TMEM slot (2): S and dP in TMEM
-  kDqBarPFull = 11,   // +TMEM slot (2): dS written (4 row warps arrive)
-  kDqBarDone = 13,    // every MMA done: dQ final
-  kDqBarDrain = 14,
+  kDqBarQ = 0,                             // Q and dO in TMEM (4 row warps arrive)
+  kDqBarKVFull = 1,                        // +slot: K and V sub-tiles landed
+  kDqBarKVEmpty = 1 + kDqSlots,            // +slot: MMAs done with the slot
+  kDqBarSFull = 1 + 2 * kDqSlots,          // +TMEM slot (2): S and dP in TMEM
+  kDqBarPFull = kDqBarSFull + 2,           // +TMEM slot (2): dS written (4 row warps arrive)
+  kDqBarDone = kDqBarPFull + 2,            // every MMA done: dQ final
+  kDqBarDrain = kDqBarDone + 1,
 };
 
 // 64-key K/V sub-tiles of rank r's lap, blocks in ring order (r - t) mod n.
@@ -479,11 +480,10 @@ struct KvWalk {
   }
 };
 
-// tq, to: Q and dO with 128-row boxes; tk64, tv64: K and V with 64-row boxes
+// tk64, tv64: K and V with 64-row boxes
 template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1)
-    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk64,
-                          const __grid_constant__ CUtensorMap tv64, const __grid_constant__ CUtensorMap to,
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tk64, const __grid_constant__ CUtensorMap tv64,
                           const __grid_constant__ BwdArgs a) {
   using L = DqSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -514,7 +514,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   }
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), (i == kDqBarPFull || i == kDqBarPFull + 1) ? 4 : 1);
+    for (int i = 0; i < L::kNumBars; ++i)
+      mbar_init(bar(i), (i == kDqBarQ || i == kDqBarPFull || i == kDqBarPFull + 1) ? 4 : 1);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -532,22 +533,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     // ===================== TMA producer =====================
     const bool leader = elect_one();
     if (leader) {
-      tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk64);
       tma_prefetch_desc(&tv64);
-      tma_prefetch_desc(&to);
-      mbar_arrive_expect_tx(bar(kDqBarQ), 2 * L::kTile);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_4d(sb + L::kOffQ + c * (kT * 128), &tq, bar(kDqBarQ), c * 64, h, q0, b);
-        tma_load_4d(sb + L::kOffO + c * (kT * 128), &to, bar(kDqBarQ), c * 64, h, q0, b);
-      }
     }
-    int issued[kSlots] = {0, 0, 0, 0};
+    int issued[kDqSlots] = {};
     KvWalk cur;
     cur.init(a, r);
     for (int j = 0; j < NJ; ++j) {
-      const int s = j & (kSlots - 1);
-      const uint32_t ph = (j >> 2) & 1;
+      const int s = j % kDqSlots;
+      const uint32_t ph = (j / kDqSlots) & 1;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(kDqBarKVEmpty + s), ph ^ 1, abort_flag, a.err, tmo)))
         break;
       if (leader) {
@@ -564,8 +558,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     }
     if (*abort_flag) {
       // let every issued copy land before the CTA's shared memory goes away
-      drain_wait_b(bar(kDqBarQ), 0, tmo);
-      for (int s = 0; s < kSlots; ++s)
+      for (int s = 0; s < kDqSlots; ++s)
         if (issued[s]) drain_wait_b(bar(kDqBarKVFull + s), (issued[s] - 1) & 1, tmo);
     }
   } else if (warp == 1) {
@@ -573,15 +566,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const bool leader = elect_one();
     constexpr uint32_t idesc_s = idesc_bf16_f32(kT, kSub, false, false);  // S, dP: M = query rows, N = 64 keys
     constexpr uint32_t idesc_q = idesc_bf16_f32(kT, D, false, true);      // dQ: A (dS) in TMEM, B (K) MN-major
-    const uint64_t q_km = smem_desc_sw128(sb + L::kOffQ, 16, 1024);
-    const uint64_t o_km = smem_desc_sw128(sb + L::kOffO, 16, 1024);
     const uint64_t k_km = smem_desc_sw128(sb + L::kOffK, 16, 1024);
     const uint64_t v_km = smem_desc_sw128(sb + L::kOffV, 16, 1024);
     const uint64_t k_mn = smem_desc_sw128(sb + L::kOffK, L::kHalfS, 1024);
-    const uint32_t km_hi = static_cast<uint32_t>(q_km >> 32), mn_hi = static_cast<uint32_t>(k_mn >> 32);
-    const uint32_t q_lo = static_cast<uint32_t>(q_km), o_lo = static_cast<uint32_t>(o_km);
+    const uint32_t km_hi = static_cast<uint32_t>(k_km >> 32), mn_hi = static_cast<uint32_t>(k_mn >> 32);
     const uint32_t k_lo = static_cast<uint32_t>(k_km), v_lo = static_cast<uint32_t>(v_km);
     const uint32_t k_mn_lo = static_cast<uint32_t>(k_mn);
+    const uint32_t t_q = tmem + 384, t_o = tmem + 384 + D / 2;  // Q and dO rows in TMEM (8 columns per K step)
     auto commit = [&](uint32_t bar_addr) {
       if (leader) mma_commit(bar_addr);
     };
@@ -591,13 +582,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const uint32_t d = tmem + ts * 128;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        if (leader) mma_ss_lohi(d, q_lo + kstep128(kk), km_hi, k_lo + slot + kstep64(kk), km_hi, idesc_s, kk > 0);
+        if (leader) mma_ts_lohi(d, t_q + kk * 8, k_lo + slot + kstep64(kk), km_hi, idesc_s, kk > 0 ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        if (leader) mma_ss_lohi(d + kSub, o_lo + kstep128(kk), km_hi, v_lo + slot + kstep64(kk), km_hi, idesc_s, kk > 0);
+        if (leader) mma_ts_lohi(d + kSub, t_o + kk * 8, v_lo + slot + kstep64(kk), km_hi, idesc_s, kk > 0 ? 1u : 0u);
     };
     auto wait_kv = [&](int j) -> bool {
-      return mbar_wait_bounded(bar(kDqBarKVFull + (j & (kSlots - 1))), (j >> 2) & 1, abort_flag, a.err, tmo);
+      return mbar_wait_bounded(bar(kDqBarKVFull + (j % kDqSlots)), (j / kDqSlots) & 1, abort_flag, a.err, tmo);
     };
     bool ok = mbar_wait_bounded(bar(kDqBarQ), 0, abort_flag, a.err, tmo);
     for (int j = 0; ok && j < 2 && j < NJ; ++j) {
@@ -611,7 +602,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     }
     // sub-step j: dQ += dS K once dS is in TMEM slot j mod 2 (K = keys: 16 key
     // rows = 2048 bytes of the MN-major sub-tile), then S, dP of sub-step j + 2
-    // into the same slot; instantiated per smem slot
+    // into the same slot; instantiated per smem slot (kDqSlots is even, so the
+    // TMEM slot is the smem slot's parity)
+    static_assert(kDqSlots % 2 == 0, "TMEM slot = smem slot parity");
     auto step = [&](auto q_c, int j) -> bool {
       constexpr int q = decltype(q_c)::value;
       constexpr int ts = q & 1;
@@ -626,16 +619,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       if (j + 2 < NJ) {
         if (!wait_kv(j + 2)) return false;
         tc_fence_after();
-        issue_sdp((q + 2) & (kSlots - 1), ts);
+        issue_sdp((q + 2) % kDqSlots, ts);
         commit(bar(kDqBarSFull + ts));
       }
       return true;
     };
-    for (int j = 0; ok && j < NJ; j += kSlots) {
+    for (int j = 0; ok && j < NJ; j += kDqSlots) {
       ok = step(std::integral_constant<int, 0>{}, j);
       if (ok && j + 1 < NJ) ok = step(std::integral_constant<int, 1>{}, j + 1);
       if (ok && j + 2 < NJ) ok = step(std::integral_constant<int, 2>{}, j + 2);
       if (ok && j + 3 < NJ) ok = step(std::integral_constant<int, 3>{}, j + 3);
+      if (ok && j + 4 < NJ) ok = step(std::integral_constant<int, 4>{}, j + 4);
+      if (ok && j + 5 < NJ) ok = step(std::integral_constant<int, 5>{}, j + 5);
     }
     if (ok) {
       commit(bar(kDqBarDone));
@@ -657,6 +652,33 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const float l = a.lse[o];
       nl2 = l == -INFINITY ? -INFINITY : -l * kLog2eB;
       ndl = -a.delta[o];
+    }
+    // this row's Q and dO into TMEM as the A operand of S and dP: column c
+    // holds elements 2c and 2c + 1 of the row, which is the row's memory
+    // read as 32-bit words; rows past the shard are zero (they take no part)
+    {
+      const int64_t ro = b * a.bstride + static_cast<int64_t>(q0 + row) * a.sstride + static_cast<int64_t>(h) * D;
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(g == 0 ? a.q : a.dout) + ro);
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t w[32];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            const uint4 u = row < nq ? src[c * 8 + x] : make_uint4(0u, 0u, 0u, 0u);
+            w[4 * x] = u.x;
+            w[4 * x + 1] = u.y;
+            w[4 * x + 2] = u.z;
+            w[4 * x + 3] = u.w;
+          }
+          tmem_st32(tmem + lane_off + 384 + g * (D / 2) + c * 32, w);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kDqBarQ));
     }
     bool ok = true;
     KvWalk cur;
@@ -744,7 +766,7 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a, const BwdTensorMaps& m, cudaStream
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.q_prefix[a.n] > 0) {
-    attn_bwd_dq_tc_kernel<D><<<dim3(a.q_prefix[a.n], a.H, a.B), kThreadsB, LQ::kAlloc, s>>>(m.q, m.k64, m.v64, m.o, a);
+    attn_bwd_dq_tc_kernel<D><<<dim3(a.q_prefix[a.n], a.H, a.B), kThreadsB, LQ::kAlloc, s>>>(m.k64, m.v64, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

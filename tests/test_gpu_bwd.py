@@ -73,6 +73,10 @@ def run_bwd(q, k, v, out, dout, lse, scale, R, U, ev=False):
     (1, 1000, 5, 128, 1, 4, True, "bf16"),    # Ulysses Anything: heads 2/1/1/1, tokens 250 x 4
     (2, 333, 7, 128, 1, 3, True, "bf16"),     # Ulysses Anything: heads 3/2/2, tokens 111 x 3
     (2, 97, 6, 64, 1, 4, True, "f32"),        # Ulysses Anything on the CUDA cores: heads 2/2/1/1, tokens 25/24/24/24
+    # the tensor-core kernels walk 64-row sub-steps through 4 (dk/dv) and 6 (dq) streamed slots:
+    (1, 130, 2, 128, 1, 1, False, "bf16"),    # an odd count of sub-steps (64 + 64 + 2)
+    (1, 700, 3, 128, 2, 1, False, "bf16"),    # 350-token shards: 12 sub-steps per lap, every slot reused
+    (1, 1000, 2, 64, 4, 1, False, "bf16"),    # ring 4 over 250-token shards at D = 64: 16 sub-steps
 ])
 def test_bwd_matches_oracle(B, S, H, D, R, U, ev, dtype):
     q, k, v = make_qkv(B, H, S, D, dtype, seed=40 + S)
