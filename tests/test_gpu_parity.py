@@ -443,6 +443,89 @@ def test_mask_all_ones_is_bitwise_unmasked_and_ring_anything_rejects_a_mask():
     assert torch.equal(ref[0], got[0]) and torch.equal(ref[1], got[1])
 
 
+@pytest.mark.parametrize("B,H,S,D,R,U", [
+    (1, 24, 4608, 128, 1, 4),   # FLUX Ulysses 4
+    (2, 8, 640, 128, 1, 2),     # two batch entries
+    (1, 12, 1024, 64, 2, 2),    # unified 2 x 2 at D = 64
+    (1, 30, 516, 128, 1, 6),    # six head groups
+])
+def test_ulysses_equals_composition_of_public_calls(B, H, S, D, R, U):
+    """The fused Ulysses call gives, bit for bit, the plain sequence of the public calls: seq->head
+    regroup of the rank shards, attention of the head groups (the ring lap inside, for the unified
+    grid), head->seq regroup of out and a permute of lse."""
+    q, k, v = dev(*make_qkv(B, H, S, D, "bf16", seed=5 + S + U))
+    scale = D ** -0.5
+    out = torch.empty((B, S, H, D), device="cuda")
+    lse = torch.empty((B, H, S), device="cuda")
+    cpa().cp_attention_fwd(q, k, v, out, lse, scale, R, U, mode="fused")
+    Hg = H // U
+
+    def to_heads(x):  # global [B, S, H, D] -> the head groups [U, B, S, Hg, D], through the rank shards
+        shards = x.view(B, U, S // U, H, D).permute(1, 0, 2, 3, 4).contiguous()
+        y = torch.empty((U, B, S, Hg, D), dtype=x.dtype, device="cuda")
+        cpa().cp_ulysses_seq2head(shards, y)
+        return y
+
+    qh, kh, vh = (to_heads(t).view(U * B, S, Hg, D) for t in (q, k, v))
+    oh = torch.empty((U * B, S, Hg, D), device="cuda")
+    lh = torch.empty((U * B, Hg, S), device="cuda")
+    if R == 1:
+        cpa().cp_block_attn_fwd(qh, kh, vh, oh, lh, scale)
+    else:
+        cpa().cp_attention_fwd(qh, kh, vh, oh, lh, scale, R, 1, mode="fused")
+    shards = torch.empty((U, B, S // U, H, D), device="cuda")
+    cpa().cp_ulysses_head2seq(oh.view(U, B, S, Hg, D), shards)
+    out_seq = shards.permute(1, 0, 2, 3, 4).reshape(B, S, H, D)
+    lse_seq = lh.view(U, B, Hg, S).permute(1, 0, 2, 3).reshape(B, H, S)
+    torch.cuda.synchronize()
+    assert cpa().cp_check_device_status() == 0
+    assert torch.equal(out, out_seq) and torch.equal(lse, lse_seq)
+
+
+@pytest.mark.parametrize("B,H,S,D,U", [(1, 24, 4481, 128, 4), (2, 7, 333, 64, 3), (1, 24, 4608, 128, 5)])
+def test_ulysses_anything_equals_composition_of_public_calls(B, H, S, D, U):
+    """The same for the ragged groups of Ulysses Anything: the ragged regroups, then the attention of
+    each head group on its own (its real heads only), then the ragged regroup back."""
+    q, k, v = dev(*make_qkv(B, H, S, D, "bf16", seed=9 + S + U))
+    scale = D ** -0.5
+    out = torch.empty((B, S, H, D), device="cuda")
+    lse = torch.empty((B, H, S), device="cuda")
+    cpa().cp_attention_fwd(q, k, v, out, lse, scale, 1, U, True, mode="fused")
+    hl = [H // U + (1 if g < H % U else 0) for g in range(U)]
+    sl = [S // U + (1 if u < S % U else 0) for u in range(U)]
+    so = [sum(sl[:u]) for u in range(U)]
+    n = B * S * H * D
+
+    def to_heads(x):  # global [B, S, H, D] -> rank blocks [B, S_u, H, D] -> group blocks [B, S, H_g, D]
+        ranks = torch.cat([x[:, so[u]:so[u] + sl[u]].reshape(-1) for u in range(U)])
+        y = torch.empty(n, dtype=x.dtype, device="cuda")
+        cpa().cp_ulysses_anything_seq2head(ranks, y, U, B, S, H, D)
+        return y
+
+    qh, kh, vh = (to_heads(t) for t in (q, k, v))
+    oh = torch.empty(n, device="cuda")
+    lses = []
+    o0 = 0
+    for g in range(U):
+        m = B * S * hl[g] * D
+        blk = [t[o0:o0 + m].view(B, S, hl[g], D) for t in (qh, kh, vh, oh)]
+        lg = torch.empty((B, hl[g], S), device="cuda")
+        cpa().cp_block_attn_fwd(blk[0], blk[1], blk[2], blk[3], lg, scale)
+        lses.append(lg)
+        o0 += m
+    ranks = torch.empty(n, device="cuda")
+    cpa().cp_ulysses_anything_head2seq(oh, ranks, U, B, S, H, D)
+    blocks, o0 = [], 0
+    for u in range(U):  # rank blocks back to the global [B, S, H, D]
+        blocks.append(ranks[o0:o0 + B * sl[u] * H * D].view(B, sl[u], H, D))
+        o0 += B * sl[u] * H * D
+    out_seq = torch.cat(blocks, dim=1)
+    torch.cuda.synchronize()
+    assert cpa().cp_check_device_status() == 0
+    assert torch.equal(out, out_seq)
+    assert torch.equal(lse, torch.cat(lses, dim=1))
+
+
 def test_cp_attention_modes_agree_and_deterministic():
     w = WORKLOADS["flux_ring4"]
     q, k, v = dev(*make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.seed))
