@@ -729,8 +729,19 @@ cp_status cp_attention_fwd_host(const void* q, const void* k, const void* v, flo
   if ((st = shard_table(S, R, uneven_ok != 0, off, len)) != CP_OK) return st;
   RingGeom g;
   fill_geom(&g, dt, R, off, len, R, off, len, -1);
+  // head chunks of decreasing size: the copies up are the bottleneck, and
+  // what follows the last chunk's copy (its attention, its copy back) is
+  // exposed, so the last chunk gets about a third of an even share and the
+  // other chunks split the rest evenly
   std::vector<int> ho(chunks), hl(chunks);
-  if (shard_table(H, chunks, true, ho.data(), hl.data()) != CP_OK) return CP_ERR_INVALID_ARG;
+  {
+    int last = chunks > 1 ? (H + 3 * chunks / 2) / (3 * chunks) : H;
+    if (last < 1) last = 1;
+    if (H - last < chunks - 1) last = H - (chunks - 1);
+    if (chunks > 1 && shard_table(H - last, chunks - 1, true, ho.data(), hl.data()) != CP_OK) return CP_ERR_INVALID_ARG;
+    ho[chunks - 1] = H - last;
+    hl[chunks - 1] = last;
+  }
   const size_t row_b = static_cast<size_t>(H) * D * eb, row4 = static_cast<size_t>(H) * D * 4;
   // copies start after everything already queued on the caller's stream
   if (cudaEventRecord(p->start, s) != cudaSuccess || cudaStreamWaitEvent(p->in, p->start, 0) != cudaSuccess ||

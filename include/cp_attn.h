@@ -250,7 +250,8 @@ cp_status cp_attention_fwd_masked(const void* q, const void* k, const void* v, c
  * aligned, caller-owned) must hold cp_attention_host_buffer_size(...) bytes:
  * device copies of q, k, v, out, lse and the workspace of cp_attention_fwd.
  * With ulysses_degree == 1 and the fused lap (or ring_degree == 1), the
- * heads are split into head_chunks balanced ranges (at most 16): chunk j's
+ * heads are split into head_chunks ranges (at most 16; the last range about
+ * a third of an even share, the others an even split of the rest): chunk j's
  * q, k, v are copied in on a library copy stream while chunk j-1 computes on
  * `stream`, and its out, lse are copied back on a second library copy stream
  * while later chunks compute, so the transfers overlap each other and the
