@@ -19,8 +19,10 @@
 //   4. dK  += dS^T Q     (A = dS^T in TMEM, B = Q MN-major)
 // S^T and dP^T of sub-step j sit in TMEM slot j mod 2 (columns [0, 64) and
 // [64, 128) of the slot); dV and dK in [256, 256 + D) and [256 + D, 256 + 2D).
-// Between 2 and 3 the row warpgroup (one thread per key row) turns S^T and
-// dP^T into P^T and dS^T (bf16, over the first 32 columns of each). The MMAs
+// Between 2 and 3 the row warps (one thread per key row and column half)
+// turn S^T and dP^T into P^T and dS^T (bf16: the 32 query columns of a half
+// over the first 16 TMEM columns of that half, so that the two halves never
+// write where the other reads). The MMAs
 // 1 and 2 of sub-step j + 2 are issued right after 3 and 4 of sub-step j, so
 // they run while the row pass works on sub-step j + 1. Q, dO, lse and delta
 // stream through four 64-row slots. After the last sub-tile it writes dk, dv.
@@ -29,12 +31,15 @@
 // in TMEM once, and walks the 64-key K/V sub-tiles of its rank's lap in ring
 // order ((r - t) mod n): S = Q K^T and dP = dO V^T (N = 64, A read from
 // TMEM) into TMEM slot j mod 2, then dQ += dS K with dS (a thread per query
-// row) over S's first 32 columns; dq is stored once. It recomputes S and dP, 1.4x the MMA work of a single fused kernel,
-// in exchange for no reduction of dq tiles across key-tile CTAs. K and V
-// stream through four 64-row slots.
+// row and column half, over the first 16 columns of each 32-column half of
+// S); dq is stored once. It recomputes S and dP, 1.4x the MMA work of a single
+// fused kernel, in exchange for no reduction of dq tiles across key-tile
+// CTAs. K and V stream through six 64-row slots.
 //
-// Warp roles (192 threads): 0 = TMA producer, 1 = MMA issuer, 2-5 = the
-// thread-per-row warpgroup (a warp reaches TMEM lanes 32 (warp mod 4) and up).
+// Warp roles (320 threads): 0 = TMA producer, 1 = MMA issuer, 2-9 = row warps:
+// a warp reaches TMEM lanes 32 (warp mod 4) and up, so two warps share each
+// lane quarter, warps 2-5 taking the first 32 columns of a sub-step and warps
+// 6-9 the other 32.
 // Every wait is bounded; on expiry the CTA records a timeout, lets its copies
 // land, frees its tensor memory and returns.
 #include <cuda.h>
@@ -50,7 +55,8 @@
 namespace cp {
 namespace {
 
-constexpr int kThreadsB = 192;
+constexpr int kRowWarps = 8;  // two per TMEM lane quarter, one per 32-column half of a sub-step
+constexpr int kThreadsB = 64 + 32 * kRowWarps;
 constexpr uint32_t kTmemColsB = 512;
 constexpr int kT = kBwdTcTile;  // keys per dk/dv CTA, query rows per dq CTA
 constexpr int kSub = 64;        // rows of a streamed sub-tile: query rows (dk/dv) or keys (dq) per sub-step
@@ -92,7 +98,7 @@ enum : int {
   kBarQFull = 1,   // +slot (4): Q, dO, lse, delta of a sub-tile landed (TMA bytes)
   kBarQEmpty = 5,  // +slot (4): MMAs done with the slot
   kBarSFull = 9,   // +TMEM slot (2): S^T and dP^T of the sub-step in TMEM
-  kBarPFull = 11,  // +TMEM slot (2): P^T, dS^T written (4 row warps arrive)
+  kBarPFull = 11,  // +TMEM slot (2): P^T, dS^T written (every row warp arrives)
   kBarDone = 13,   // every MMA of the CTA done: dK, dV final
   kBarDrain = 14,
 };
@@ -118,7 +124,6 @@ struct QCursor {
     }
   }
   __device__ __forceinline__ int q0() const { return off + tile * kSub; }
-  __device__ __forceinline__ int nvalid() const { return min(kSub, len - tile * kSub); }
   __device__ __forceinline__ void advance(const BwdArgs& a, int jb) {
     if (++tile >= ntile) next_block(a, jb);
   }
@@ -131,6 +136,11 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity, uint
 }
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+// TMEM column (within S's or dP's 64) of the bf16 A operand for K step kk of
+// a sub-step: rows [32 h, 32 h + 32) of the sub-step (written by the row warps
+// of column half h) sit in columns [32 h, 32 h + 16), 8 columns per K step
+__device__ __forceinline__ uint32_t pcol(int kk) { return static_cast<uint32_t>((kk >> 1) * 32 + (kk & 1) * 8); }
 
 // tq64, to64: Q and dO with 64-row boxes; tk, tv: K and V with 128-row boxes
 template <int D>
@@ -170,7 +180,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
       const bool four = i == kBarPFull || i == kBarPFull + 1;
-      mbar_init(bar(i), four ? 4 : 1);
+      mbar_init(bar(i), four ? kRowWarps : 1);
     }
     misc[1] = 0;
     fence_mbar_init();
@@ -261,17 +271,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           mma_ss_lohi(d + kSub, v_km_lo + kstep128(kk), km_hi, o_km_lo + slot + kstep64(kk), km_hi, idesc_s, kk > 0);
     };
     // dV += P^T dO and dK += dS^T Q over the sub-tile's 64 query rows (K = rows:
-    // 16 rows = 2048 bytes of an MN-major sub-tile)
+    // 16 rows = 2048 bytes of an MN-major sub-tile; the bf16 P^T / dS^T of
+    // rows [32 h, 32 h + 32) sit in TMEM columns [32 h, 32 h + 16) of theirs)
     auto issue_g = [&](int q, int ts, bool acc) {
       const uint32_t slot = static_cast<uint32_t>((q * L::kSubT) >> 4);
       const uint32_t pa = tmem + ts * 128;
 #pragma unroll
       for (int kk = 0; kk < kSub / 16; ++kk)
-        if (leader) mma_ts_lohi(tmem + 256, pa + kk * 8, o_mn_lo + slot + ((kk * 2048) >> 4), mn_hi, idesc_g,
+        if (leader) mma_ts_lohi(tmem + 256, pa + pcol(kk), o_mn_lo + slot + ((kk * 2048) >> 4), mn_hi, idesc_g,
                                 (acc || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < kSub / 16; ++kk)
-        if (leader) mma_ts_lohi(tmem + 256 + D, pa + kSub + kk * 8, q_mn_lo + slot + ((kk * 2048) >> 4), mn_hi,
+        if (leader) mma_ts_lohi(tmem + 256 + D, pa + kSub + pcol(kk), q_mn_lo + slot + ((kk * 2048) >> 4), mn_hi,
                                 idesc_g, (acc || kk > 0) ? 1u : 0u);
     };
     auto wait_q = [&](int j) -> bool {
@@ -319,8 +330,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       drain_wait_b(bar(kBarDrain), 0, tmo);
     }
   } else {
-    // ===================== row pass: one thread per key row =====================
+    // ===================== row pass: one thread per key row and column half =====================
     const int wq = warp & 3;
+    const int hc = (warp - 2) >> 2;  // this warp's 32 query columns of each sub-step
     const int key = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const bool kvalid = key < nk;
@@ -336,8 +348,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const uint32_t t_s = tmem + lane_off + ts * 128, t_dp = t_s + kSub;
       const float* lse2 = s_lse + q * kSub;
       const float* dlt = s_dlt + q * kSub;
-#pragma unroll 1
-      for (int c = 0; c < kSub / 32; ++c) {
+      {
+        const int c = hc;
         uint32_t sr[32], dr[32];
         tmem_ld32(t_s + c * 32, sr);
         tmem_ld32(t_dp + c * 32, dr);
@@ -368,9 +380,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
           for (int x = 0; x < 16; ++x) pp[x] = dd[x] = 0u;  // a key past the tile: p = ds = 0
         }
-        // P^T over S^T's consumed columns, dS^T over dP^T's consumed columns
-        tmem_st16(t_s + c * 16, pp);
-        tmem_st16(t_dp + c * 16, dd);
+        // P^T over the first half of this warp's S^T columns, dS^T over those of dP^T
+        tmem_st16(t_s + c * 32, pp);
+        tmem_st16(t_dp + c * 32, dd);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -382,8 +394,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     if (ok) {
       tc_fence_after();
       const int64_t o = b * a.bstride + static_cast<int64_t>(key0 + key) * a.sstride + h * D;
-#pragma unroll 1
-      for (int g = 0; g < 2; ++g) {
+      {
+        const int g = hc;  // column half 0 writes dv, half 1 dk
         float* dst = g == 0 ? a.dv : a.dk;
         const float mul = g == 0 ? 1.f : a.scale;
 #pragma unroll 1
@@ -423,9 +435,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 //   dQ += dS K    (TS: dS over S's first 32 columns, K read MN-major)
 //                                                    -> TMEM [256, 256 + D)
 // Only K and V come from shared memory. S and dP of sub-step j + 2 are issued
-// right after dQ of sub-step j, so they run while warps 2-5 (one thread per
-// query row, lse and delta in registers) form dS = p (dp - delta) of
-// sub-step j + 1. dq is stored once, without atomics.
+// right after dQ of sub-step j, so they run while the row warps (one thread
+// per query row and column half, lse and delta in registers) form
+// dS = p (dp - delta) of sub-step j + 1. dq is stored once, without atomics.
 // ----------------------------------------------------------------------------
 constexpr int kDqSlots = 6;  // K/V sub-tile slots of the dq kernel
 
@@ -444,11 +456,11 @@ struct DqSmem {
 };
 
 enum : int {
-  kDqBarQ = 0,                             // Q and dO in TMEM (4 row warps arrive)
+  kDqBarQ = 0,                             // Q and dO in TMEM (every row warp arrives)
   kDqBarKVFull = 1,                        // +slot: K and V sub-tiles landed
   kDqBarKVEmpty = 1 + kDqSlots,            // +slot: MMAs done with the slot
   kDqBarSFull = 1 + 2 * kDqSlots,          // +TMEM slot (2): S and dP in TMEM
-  kDqBarPFull = kDqBarSFull + 2,           // +TMEM slot (2): dS written (4 row warps arrive)
+  kDqBarPFull = kDqBarSFull + 2,           // +TMEM slot (2): dS written (every row warp arrives)
   kDqBarDone = kDqBarPFull + 2,            // every MMA done: dQ final
   kDqBarDrain = kDqBarDone + 1,
 };
@@ -515,7 +527,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
-      mbar_init(bar(i), (i == kDqBarQ || i == kDqBarPFull || i == kDqBarPFull + 1) ? 4 : 1);
+      mbar_init(bar(i), (i == kDqBarQ || i == kDqBarPFull || i == kDqBarPFull + 1) ? kRowWarps : 1);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -613,7 +625,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const uint32_t slot = static_cast<uint32_t>((q * L::kSubT) >> 4);
 #pragma unroll
       for (int kk = 0; kk < kSub / 16; ++kk)
-        if (leader) mma_ts_lohi(tmem + 256, tmem + ts * 128 + kk * 8, k_mn_lo + slot + ((kk * 2048) >> 4), mn_hi,
+        if (leader) mma_ts_lohi(tmem + 256, tmem + ts * 128 + pcol(kk), k_mn_lo + slot + ((kk * 2048) >> 4), mn_hi,
                                 idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
       commit(bar(kDqBarKVEmpty + q));
       if (j + 2 < NJ) {
@@ -639,8 +651,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       drain_wait_b(bar(kDqBarDrain), 0, tmo);
     }
   } else {
-    // ===================== dS: one thread per query row =====================
+    // ===================== dS: one thread per query row and column half =====================
     const int wq = warp & 3;
+    const int hc = (warp - 2) >> 2;  // this warp's 32 key columns of each sub-step
     const int row = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float c2 = a.scale * kLog2eB;
@@ -653,13 +666,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       nl2 = l == -INFINITY ? -INFINITY : -l * kLog2eB;
       ndl = -a.delta[o];
     }
-    // this row's Q and dO into TMEM as the A operand of S and dP: column c
-    // holds elements 2c and 2c + 1 of the row, which is the row's memory
-    // read as 32-bit words; rows past the shard are zero (they take no part)
+    // this row's Q (column half 0) or dO (half 1) into TMEM as the A operand
+    // of S and dP: column c holds elements 2c and 2c + 1 of the row, which is
+    // the row's memory read as 32-bit words; rows past the shard are zero
+    // (they take no part)
     {
       const int64_t ro = b * a.bstride + static_cast<int64_t>(q0 + row) * a.sstride + static_cast<int64_t>(h) * D;
-#pragma unroll 1
-      for (int g = 0; g < 2; ++g) {
+      {
+        const int g = hc;
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(g == 0 ? a.q : a.dout) + ro);
 #pragma unroll 1
         for (int c = 0; c < D / 64; ++c) {
@@ -690,8 +704,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       tc_fence_after();
       const uint32_t t_s = tmem + lane_off + ts * 128, t_dp = t_s + kSub;  // this sub-step's slot
       const int nvk = cur.nvalid();
-#pragma unroll 1
-      for (int c = 0; c < kSub / 32; ++c) {
+      {
+        const int c = hc;
         uint32_t sr[32], dr[32];
         tmem_ld32(t_s + c * 32, sr);
         tmem_ld32(t_dp + c * 32, dr);
@@ -709,8 +723,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           d1 = c * 32 + e + 1 < nvk ? d1 : 0.f;
           dd[e >> 1] = pack_bf16x2(d0, d1);
         }
-        // dS over S's consumed columns
-        tmem_st16(t_s + c * 16, dd);
+        // dS over the first half of this warp's S columns
+        tmem_st16(t_s + c * 32, dd);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -724,7 +738,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       tc_fence_after();
       float* dst = a.dq + b * a.bstride + static_cast<int64_t>(q0 + row) * a.sstride + h * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = hc * (D / 64); c < (hc + 1) * (D / 64); ++c) {  // this half's D / 2 columns
         uint32_t rr[32];
         tmem_ld32(tmem + lane_off + 256 + c * 32, rr);
         tmem_wait_ld();
