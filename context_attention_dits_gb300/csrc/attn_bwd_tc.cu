@@ -143,18 +143,18 @@ __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t pcol(int kk) { return static_cast<uint32_t>((kk >> 1) * 32 + (kk & 1) * 8); }
 
 // tq64, to64: Q and dO with 64-row boxes; tk, tv: K and V with 128-row boxes
+// One dk/dv CTA: key tile bx of the lap's key tiles (kv_prefix) of head h,
+// batch entry b; smem_raw holds alloc bytes of dynamic shared memory.
 template <int D>
-__global__ void __launch_bounds__(kThreadsB, 1)
-    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tq64, const __grid_constant__ CUtensorMap tk,
-                            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to64,
-                            const __grid_constant__ BwdArgs a) {
+__device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tq64, const CUtensorMap& tk, const CUtensorMap& tv,
+                                             const CUtensorMap& to64, const BwdArgs& a, uint8_t* smem_raw, int alloc,
+                                             int bx, int h, int b) {
   using L = BSmem<D>;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the swizzled tiles need a 1024-byte aligned base; a base that would need
   // more padding than the allocation holds is reported (uniformly, before any
   // barrier or TMEM use) instead of used
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
-  if (pad > static_cast<uint32_t>(L::kAlloc - L::kBytes)) {
+  if (pad > static_cast<uint32_t>(alloc - L::kBytes)) {
     if (threadIdx.x == 0) atomicOr(a.err, kDevErrLayout);
     return;
   }
@@ -168,11 +168,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   float* s_lse = reinterpret_cast<float*>(smem + L::kOffLse);
   float* s_dlt = reinterpret_cast<float*>(smem + L::kOffDlt);
 
-  const int h = blockIdx.y, b = blockIdx.z;
   if (bwd_head_is_padding(a, h, b)) return;  // uniform per CTA, before any barrier or TMEM
   int jb = 0;
-  while (jb + 1 < a.n && a.kv_prefix[jb + 1] <= static_cast<int>(blockIdx.x)) ++jb;
-  const int key0 = a.off[jb] + (static_cast<int>(blockIdx.x) - a.kv_prefix[jb]) * kT;
+  while (jb + 1 < a.n && a.kv_prefix[jb + 1] <= bx) ++jb;
+  const int key0 = a.off[jb] + (bx - a.kv_prefix[jb]) * kT;
   const int nk = min(kT, a.off[jb] + a.len[jb] - key0);
   int NJ = 0;  // 64-row query sub-steps of the lap
   for (int t = 0; t < a.n; ++t) NJ += (a.len[(jb + t) % a.n] + kSub - 1) / kSub;
@@ -492,15 +491,14 @@ struct KvWalk {
   }
 };
 
-// tk64, tv64: K and V with 64-row boxes
+// One dq CTA: query tile bx of the lap's query tiles (q_prefix) of head h,
+// batch entry b. tk64, tv64: K and V with 64-row boxes.
 template <int D>
-__global__ void __launch_bounds__(kThreadsB, 1)
-    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tk64, const __grid_constant__ CUtensorMap tv64,
-                          const __grid_constant__ BwdArgs a) {
+__device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tk64, const CUtensorMap& tv64, const BwdArgs& a,
+                                           uint8_t* smem_raw, int alloc, int bx, int h, int b) {
   using L = DqSmem<D>;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
-  if (pad > static_cast<uint32_t>(L::kAlloc - L::kBytes)) {
+  if (pad > static_cast<uint32_t>(alloc - L::kBytes)) {
     if (threadIdx.x == 0) atomicOr(a.err, kDevErrLayout);
     return;
   }
@@ -512,11 +510,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   volatile uint32_t* abort_flag = misc + 1;
   auto bar = [&](int i) -> uint32_t { return sb + L::kOffBar + 8 * i; };
 
-  const int h = blockIdx.y, b = blockIdx.z;
   if (bwd_head_is_padding(a, h, b)) return;  // uniform per CTA, before any barrier or TMEM
   int r = 0;
-  while (r + 1 < a.n && a.q_prefix[r + 1] <= static_cast<int>(blockIdx.x)) ++r;
-  const int q0 = a.off[r] + (static_cast<int>(blockIdx.x) - a.q_prefix[r]) * kT;
+  while (r + 1 < a.n && a.q_prefix[r + 1] <= bx) ++r;
+  const int q0 = a.off[r] + (bx - a.q_prefix[r]) * kT;
   const int nq = min(kT, a.off[r] + a.len[r] - q0);
   int NJ = 0;  // 64-key sub-steps of the lap
   for (int t = 0; t < a.n; ++t) {
@@ -764,26 +761,43 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 }
 
 template <int D>
+__host__ __device__ constexpr int bwd_tc_alloc() {
+  return BSmem<D>::kAlloc > DqSmem<D>::kAlloc ? BSmem<D>::kAlloc : DqSmem<D>::kAlloc;
+}
+
+// Both kinds of CTA in one launch, the dk/dv CTAs (the longer ones) first:
+// the dq CTAs then fill the SMs that the last wave of dk/dv CTAs leaves idle,
+// and neither kind waits for the other's tail. The two kinds are independent
+// (they read the same inputs and write dk, dv or dq).
+template <int D>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq64, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to64,
+                       const __grid_constant__ CUtensorMap tk64, const __grid_constant__ CUtensorMap tv64,
+                       const __grid_constant__ BwdArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int nkv = a.kv_prefix[a.n], nq = a.q_prefix[a.n];
+  const int kv_ctas = nkv * a.H * a.B;
+  const int id = static_cast<int>(blockIdx.x);
+  if (id < kv_ctas) {
+    bwd_dkdv_cta<D>(tq64, tk, tv, to64, a, smem_raw, bwd_tc_alloc<D>(), id % nkv, (id / nkv) % a.H, id / (nkv * a.H));
+  } else {
+    const int i = id - kv_ctas;
+    bwd_dq_cta<D>(tk64, tv64, a, smem_raw, bwd_tc_alloc<D>(), i % nq, (i / nq) % a.H, i / (nq * a.H));
+  }
+}
+
+template <int D>
 cudaError_t launch_bwd_tc_d(const BwdArgs& a, const BwdTensorMaps& m, cudaStream_t s) {
-  using L = BSmem<D>;
-  using LQ = DqSmem<D>;
-  static_assert(L::kAlloc <= 227 * 1024 && LQ::kAlloc <= 227 * 1024, "shared memory budget");
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  constexpr int kAlloc = bwd_tc_alloc<D>();
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LQ::kAlloc);
-  if (e != cudaSuccess) return e;
-  if (a.H == 0 || a.B == 0) return cudaSuccess;
-  if (a.kv_prefix[a.n] > 0) {
-    attn_bwd_dkdv_tc_kernel<D>
-        <<<dim3(a.kv_prefix[a.n], a.H, a.B), kThreadsB, L::kAlloc, s>>>(m.q64, m.k, m.v, m.o64, a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  if (a.q_prefix[a.n] > 0) {
-    attn_bwd_dq_tc_kernel<D><<<dim3(a.q_prefix[a.n], a.H, a.B), kThreadsB, LQ::kAlloc, s>>>(m.k64, m.v64, a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  const int64_t ctas = (static_cast<int64_t>(a.kv_prefix[a.n]) + a.q_prefix[a.n]) * a.H * a.B;
+  if (ctas == 0) return cudaSuccess;
+  if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
+  attn_bwd_tc_kernel<D><<<static_cast<unsigned>(ctas), kThreadsB, kAlloc, s>>>(m.q64, m.k, m.v, m.o64, m.k64, m.v64, a);
+  return cudaGetLastError();
 }
 
 }  // namespace

@@ -988,9 +988,10 @@ size_t cp_attention_bwd_workspace_size(int B, int H, int S, int D, int ring_degr
 int cp_attention_bwd_launch_count(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt) {
   if (B <= 0 || S <= 0 || H < 1 || D < 1 || ring_degree < 1 || ulysses_degree < 1) return 0;
   const int U = ulysses_degree;
-  // delta, then the dk/dv and dq kernels (tensor cores for bf16, CUDA cores
-  // for fp32); bf16 adds the padded lse / delta copy of the dk/dv kernel
-  int n = dt == CP_BF16 ? 4 : 3;
+  // delta, then the dk/dv and dq kernels: on the CUDA cores (fp32) one launch
+  // each; on the tensor cores (bf16) the padded lse / delta copy of the dk/dv
+  // CTAs, then one launch of both kinds of CTA
+  int n = 3;
   if (U > 1 && U <= H) {
     const BwdWs w = bwd_ws_layout(B, H, S, D, ring_degree, U, dt);
     char* base = reinterpret_cast<char*>(uintptr_t{1} << 20);

@@ -176,18 +176,18 @@ def test_bwd_sizes_counts_and_rejects_before_launch():
     assert ws(1, 24, 4608, 128, 4, 1, torch.bfloat16) >= nl * 4                      # delta only
     assert ws(1, 24, 4608, 128, 1, 4, torch.bfloat16) >= nl * 4 + 4 * n * 2 + 2 * nl * 4 + 3 * n * 4
     c = cpa.cp_attention_bwd_launch_count
-    assert c(1, 24, 4608, 128, 4, 1, torch.bfloat16) == 4       # delta, padded lse/delta, dk/dv, dq (tensor cores)
+    assert c(1, 24, 4608, 128, 4, 1, torch.bfloat16) == 3       # delta, padded lse/delta, dk/dv + dq (tensor cores)
     assert c(1, 24, 4608, 128, 4, 1, torch.float32) == 3        # delta, dq, dk/dv on the CUDA cores
     # Ulysses: q, k, v, dout, lse, delta regroups share a launch, dq, dk, dv another
-    assert c(1, 24, 4608, 128, 1, 4, torch.bfloat16) == 6
+    assert c(1, 24, 4608, 128, 1, 4, torch.bfloat16) == 5
     assert c(0, 24, 4608, 128, 4, 1, torch.bfloat16) == 0
     # Ulysses Anything over 5 head groups: 30 ragged in-copies (two bulk launches of <= 24), 15 out-copies
-    assert c(1, 24, 4608, 128, 1, 5, torch.bfloat16) == 4 + 2 + 1
+    assert c(1, 24, 4608, 128, 1, 5, torch.bfloat16) == 3 + 2 + 1
     # 4481-float lse / delta rows are not 16-byte multiples: each of their 10 copies takes a vector launch,
     # the 20 q, k, v, dout copies share one bulk launch
-    assert c(1, 24, 4481, 128, 1, 5, torch.bfloat16) == 4 + (1 + 10) + 1
+    assert c(1, 24, 4481, 128, 1, 5, torch.bfloat16) == 3 + (1 + 10) + 1
     # 128 KB lse / delta rows exceed a ring slot at 32768 tokens
-    assert c(2, 24, 32768, 128, 2, 4, torch.bfloat16) == 4 + (1 + 2) + 1
+    assert c(2, 24, 32768, 128, 2, 4, torch.bfloat16) == 3 + (1 + 2) + 1
     # q, k, v, out, dout, lse, dq, dk, dv, B, H, S, D, scale, R, U, ev, ws, ws_bytes, dt, stream
     big = 1 << 34
     f = lambda **kw: L.cp_attention_bwd(kw.get("q", p), p, p, p, p, p, p, p, kw.get("dv", p), 1, 24,
