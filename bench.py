@@ -35,7 +35,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "context-parallel attention fwd TFLOP/s and % bf16 tensor peak on 1 GB300"
 UNIT = "TFLOP/s"
-E2E_HEAD_CHUNKS = 4  # head chunks of the host-buffer call
+E2E_HEAD_CHUNKS = 5  # head chunks of the host-buffer call
 N_SETS = 3           # input sets the timed steps rotate over (together larger than L2)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_tc_flux_ring4.md")

@@ -196,7 +196,7 @@ def cp_attention_host_buffer_size(B, H, S, D, ring_degree=1, ulysses_degree=1, d
 
 
 def cp_attention_fwd_host(q, k, v, out, lse, scale: float, ring_degree: int = 1, ulysses_degree: int = 1,
-                          uneven_ok: bool = False, dev_buffer=None, mode="fused", head_chunks: int = 4,
+                          uneven_ok: bool = False, dev_buffer=None, mode="fused", head_chunks: int = 5,
                           stream=None):
     """cp_attention_fwd over host (CPU, ideally pinned) tensors q, k, v [B,S,H,D], out [B,S,H,D] f32 and
     lse [B,H,S] f32, with transfers overlapping compute over head chunks. dev_buffer: a CUDA uint8 tensor

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -34,6 +35,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct DeviceInfo {
   int checked = 0;  // 0 unknown, 1 sm_103, -1 other
   uint32_t* err = nullptr;
+  int sms = 0;  // multiprocessors
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -49,6 +51,10 @@ cp_status current_device(DeviceInfo** out) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return CP_ERR_CUDA;
     d.checked = (major == 10 && minor == 3) ? 1 : -1;
+    if (d.checked == 1 && cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      d.checked = 0;
+      return CP_ERR_CUDA;
+    }
     if (d.checked == 1) {
       d.err = cp::device_error_word();
       if (!d.err) {
@@ -729,18 +735,41 @@ cp_status cp_attention_fwd_host(const void* q, const void* k, const void* v, flo
   if ((st = shard_table(S, R, uneven_ok != 0, off, len)) != CP_OK) return st;
   RingGeom g;
   fill_geom(&g, dt, R, off, len, R, off, len, -1);
-  // head chunks of decreasing size: the copies up are the bottleneck, and
-  // what follows the last chunk's copy (its attention, its copy back) is
-  // exposed, so the last chunk gets about a third of an even share and the
-  // other chunks split the rest evenly
+  // head chunks: the copies up are the bottleneck. What precedes the first
+  // chunk's attention (its copy up) and what follows the last chunk's copy
+  // up (its attention, its copy back) is exposed, so those two chunks get
+  // about a third of an even share each, and the middle chunks the rest,
+  // largest first, each at most one wave of work items (a launch of up to a
+  // wave takes one item's time whatever its size). Where the middle chunks
+  // cannot hold the rest within a wave each, only the last chunk is small
+  // and the others split the rest evenly.
   std::vector<int> ho(chunks), hl(chunks);
   {
-    int last = chunks > 1 ? (H + 3 * chunks / 2) / (3 * chunks) : H;
-    if (last < 1) last = 1;
-    if (H - last < chunks - 1) last = H - (chunks - 1);
-    if (chunks > 1 && shard_table(H - last, chunks - 1, true, ho.data(), hl.data()) != CP_OK) return CP_ERR_INVALID_ARG;
-    ho[chunks - 1] = H - last;
-    hl[chunks - 1] = last;
+    const int n_single = g.single_prefix[g.n_q];
+    const int64_t per_head = static_cast<int64_t>(g.pair_prefix[g.n_q] + n_single - n_single / 2) * B;
+    const int64_t wave_heads = per_head > 0 ? dinfo->sms / per_head : 0;  // heads per wave of items
+    int edge = (H + 3 * chunks / 2) / (3 * chunks);
+    if (edge < 1) edge = 1;
+    const int mids = chunks - 2, rest = H - 2 * edge;
+    if (mids >= 1 && rest >= mids && wave_heads >= 1 && wave_heads * mids >= rest) {
+      hl[0] = edge;
+      int left = rest;
+      for (int j = 1; j <= mids; ++j) {
+        hl[j] = static_cast<int>(std::min<int64_t>(wave_heads, left - (mids - j)));
+        left -= hl[j];
+      }
+      hl[chunks - 1] = edge;
+      for (int j = 0, o = 0; j < chunks; ++j) {
+        ho[j] = o;
+        o += hl[j];
+      }
+    } else {
+      int last = edge;
+      if (H - last < chunks - 1) last = H - (chunks - 1);
+      if (shard_table(H - last, chunks - 1, true, ho.data(), hl.data()) != CP_OK) return CP_ERR_INVALID_ARG;
+      ho[chunks - 1] = H - last;
+      hl[chunks - 1] = last;
+    }
   }
   const size_t row_b = static_cast<size_t>(H) * D * eb, row4 = static_cast<size_t>(H) * D * 4;
   // copies start after everything already queued on the caller's stream

@@ -250,8 +250,12 @@ cp_status cp_attention_fwd_masked(const void* q, const void* k, const void* v, c
  * aligned, caller-owned) must hold cp_attention_host_buffer_size(...) bytes:
  * device copies of q, k, v, out, lse and the workspace of cp_attention_fwd.
  * With ulysses_degree == 1 and the fused lap (or ring_degree == 1), the
- * heads are split into head_chunks ranges (at most 16; the last range about
- * a third of an even share, the others an even split of the rest): chunk j's
+ * heads are split into head_chunks ranges (at most 16). The first and the
+ * last range get about a third of an even share each and the middle ranges
+ * the rest, largest first, each at most the heads whose work items fill one
+ * wave of the device's SMs; where that does not fit, only the last range is
+ * small and the others split the rest evenly (at FLUX ring 4, 24 heads: 5
+ * chunks -> 2, 8, 8, 4, 2; 4 chunks -> 8, 7, 7, 2). Chunk j's
  * q, k, v are copied in on a library copy stream while chunk j-1 computes on
  * `stream`, and its out, lse are copied back on a second library copy stream
  * while later chunks compute, so the transfers overlap each other and the
