@@ -344,8 +344,10 @@ cp_status cp_attention_fwd_no_alloc(const void* q, const void* k, const void* v,
 size_t cp_attention_bwd_workspace_size(int B, int H, int S, int D, int ring_degree, int ulysses_degree,
                                        cp_dtype dt);
 
-/* Kernel launches one cp_attention_bwd call makes (delta, dq, dk/dv, and the
- * Ulysses regroups). 0 for empty or invalid sizes. */
+/* Kernel launches one cp_attention_bwd call makes: delta; then for bf16 the
+ * padded lse / delta copy and one launch of the dk/dv and dq CTAs, for fp32 a
+ * dq and a dk/dv launch; and the Ulysses regroups. 0 for empty or invalid
+ * sizes. */
 int cp_attention_bwd_launch_count(int B, int H, int S, int D, int ring_degree, int ulysses_degree, cp_dtype dt);
 
 /* Backward of cp_attention_fwd (ring, Ulysses, unified or Ulysses Anything).
