@@ -442,6 +442,69 @@ class ClockSampler:
                 "power_w_max": max((num(p[2]) or 0.0) for p in inside)}
 
 
+class NvmlClockSampler(ClockSampler):
+    """The same record through NVML (the driver's libnvidia-ml; read-only queries), polled about every
+    millisecond on a thread, so that a timed region of a few milliseconds still holds samples. Reason
+    bits are NVML's clock-event reasons."""
+    REASON_BITS = ((0x8, "hw_slowdown"), (0x40, "hw_thermal_slowdown"), (0x20, "sw_thermal_slowdown"),
+                   (0x4, "sw_power_cap"))
+
+    def __init__(self, gpu_uuid):  # noqa: super().__init__ would start nvidia-smi
+        import ctypes
+        self.samples, self.proc, self.window, self.stopped = [], None, None, False
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib, self.c = lib, ctypes
+        self.handle = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(str(gpu_uuid).encode(), ctypes.byref(self.handle)) != 0:
+            raise OSError("no NVML handle for " + str(gpu_uuid))
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
+
+    def _poll(self):
+        c = self.c
+        sm, mx, mw, rs = c.c_uint(), c.c_uint(), c.c_uint(), c.c_ulonglong()
+        while not self.stopped:
+            ok = (self.lib.nvmlDeviceGetClockInfo(self.handle, 1, c.byref(sm)) == 0 and
+                  self.lib.nvmlDeviceGetMaxClockInfo(self.handle, 1, c.byref(mx)) == 0 and
+                  self.lib.nvmlDeviceGetPowerUsage(self.handle, c.byref(mw)) == 0 and
+                  self.reasons_fn(self.handle, c.byref(rs)) == 0)
+            if ok:
+                flags = ["Active" if rs.value & bit else "Not Active" for bit, _ in self.REASON_BITS]
+                self.samples.append((time.time(), [str(sm.value), str(mx.value), str(mw.value / 1000.0)] + flags))
+            time.sleep(0.001)
+
+    def stop(self):
+        self.stopped = True
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, window=None):
+        # the window itself (samples are dense), else the sample nearest to it
+        t0, t1 = window or self.window or (0, float("inf"))
+        if self.samples and not any(t0 <= t <= t1 for t, _ in self.samples):
+            return super().summary(window)
+        saved = self.samples
+        self.samples = [(t, p) for t, p in saved if t0 <= t <= t1]
+        try:
+            out = super().summary((t0 - 1.0, t1 + 1.0))
+        finally:
+            self.samples = saved
+        out["source"] = "nvml, ~1 ms"
+        return out
+
+
+def clock_sampler(gpu_id):
+    """NVML polling where the driver library loads, else nvidia-smi at 100 ms."""
+    try:
+        return NvmlClockSampler(gpu_id)
+    except (OSError, AttributeError):
+        return ClockSampler(gpu_id)
+
+
 # ---------------------------------------------------------------------------
 # traffic of the dominant kernel from the committed ncu summary
 # ---------------------------------------------------------------------------
@@ -587,7 +650,7 @@ def run_ours(args, w, world, rank, local):
         gpu_id = f"GPU-{gpu_id}" if not str(gpu_id).startswith("GPU-") else str(gpu_id)
     except Exception:
         pass
-    clocks = ClockSampler(gpu_id)
+    clocks = clock_sampler(gpu_id)
     time.sleep(0.3)
 
     t_start = torch.cuda.Event(enable_timing=True)
@@ -678,7 +741,7 @@ def run_ours(args, w, world, rank, local):
             cpu = cpu_baseline(w, q_h, k_h, v_h)
         sec = None
         if world == 1 and not args.no_secondary:
-            sec_clocks = ClockSampler(gpu_id)
+            sec_clocks = clock_sampler(gpu_id)
             time.sleep(0.3)
             try:
                 sec = secondary(cpa, dev, flush, stream, peaks, sec_clocks)
