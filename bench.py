@@ -12,7 +12,9 @@ together exceed the L2 cache (so no step finds its inputs there); the
 secondary measurements flush L2 (a 512 MB write) between timed launches,
 outside their events. With N > 1 (torchrun), every rank runs its own
 independent problem on its own GPU (weak scaling, no data-path collective);
-the time is the max over ranks.
+the time is the max over ranks. Clocks, power and clock-event reasons are
+sampled inside each timed region through NVML about every millisecond
+(nvidia-smi at 100 ms where NVML does not load).
 
 Prints one JSON line (rank 0).
 """
