@@ -253,6 +253,46 @@ __global__ void __launch_bounds__(256) segment_copy_kernel(const SegCopy c, int6
   }
 }
 
+// The same copy for few, long segments: each segment is cut into `parts`
+// ranges of chunk_v vectors, and each warp copies one (segment, range) unit,
+// so that the copy spreads over the GPU instead of a few warps walking whole
+// segments.
+template <typename V>
+__global__ void __launch_bounds__(256) segment_copy_parts_kernel(const SegCopy c, int64_t parts, int64_t chunk_v) {
+  const int lane = threadIdx.x & 31;
+  const int64_t unit = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t nseg = c.n0 * c.n1 * c.n2 * c.n3;
+  if (unit >= nseg * parts) return;
+  const int64_t seg = unit / parts, part = unit - seg * parts;
+  const int64_t nv = c.seg_elems * c.elem_bytes / static_cast<int64_t>(sizeof(V));
+  const int64_t v0 = part * chunk_v, v1 = v0 + chunk_v < nv ? v0 + chunk_v : nv;
+  int64_t rest = seg;
+  const int64_t i3 = rest % c.n3;
+  rest /= c.n3;
+  const int64_t i2 = rest % c.n2;
+  rest /= c.n2;
+  const int64_t i1 = rest % c.n1, i0 = rest / c.n1;
+  const bool out_contig = (c.ost0 | c.ost1 | c.ost2 | c.ost3) == 0;
+  const int64_t src_el = i0 * c.st0 + i1 * c.st1 + i2 * c.st2 + i3 * c.st3;
+  const int64_t dst_b = out_contig ? seg * c.seg_elems * c.elem_bytes
+                                   : (i0 * c.ost0 + i1 * c.ost1 + i2 * c.ost2 + i3 * c.ost3) * c.elem_bytes;
+  const V* src = reinterpret_cast<const V*>(static_cast<const char*>(c.in) + src_el * c.elem_bytes);
+  V* dst = reinterpret_cast<V*>(static_cast<char*>(c.out) + dst_b);
+  for (int64_t base = v0; base < v1; base += 32 * kCopyVec) {
+    V x[kCopyVec];
+#pragma unroll
+    for (int j = 0; j < kCopyVec; ++j) {
+      const int64_t v = base + lane + 32 * j;
+      if (v < v1) x[j] = src[v];
+    }
+#pragma unroll
+    for (int j = 0; j < kCopyVec; ++j) {
+      const int64_t v = base + lane + 32 * j;
+      if (v < v1) dst[v] = x[j];
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 // Segment copy with bulk TMA copies. One thread per CTA walks a contiguous
 // range of output segments in chunks of K consecutive segments (K * segment
@@ -518,6 +558,22 @@ static cudaError_t launch_vector(const SegCopy& c, cudaStream_t s) {
                    reinterpret_cast<uintptr_t>(c.out);
   for (int64_t st : {c.st0, c.st1, c.st2, c.st3, c.ost0, c.ost1, c.ost2, c.ost3})
     align |= static_cast<uint64_t>(st * c.elem_bytes);
+  // few, long segments (fewer than one per resident warp, each many
+  // vector rounds): a warp per part of a segment instead
+  auto launch_parts = [&](auto kernel, int64_t vec_bytes) -> bool {
+    const int64_t nv = seg_bytes / vec_bytes;
+    const int64_t warps_cap = static_cast<int64_t>(sms) * 2 * 8;
+    const int64_t round = 32 * kCopyVec;  // vectors a warp moves per round
+    if (nseg * 4 > warps_cap || nv < 8 * round) return false;
+    int64_t parts = warps_cap / nseg;
+    if (parts > nv / (4 * round)) parts = nv / (4 * round);  // at least 4 rounds per part
+    if (parts < 2) return false;
+    const int64_t chunk_v = (nv + parts - 1) / parts;
+    parts = (nv + chunk_v - 1) / chunk_v;
+    const int64_t blocks = (nseg * parts + 7) / 8;
+    kernel<<<static_cast<int>(blocks), 256, 0, s>>>(c, parts, chunk_v);
+    return true;
+  };
   auto launch = [&](auto kernel) {
     int per_sm = 1;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
@@ -530,10 +586,14 @@ static cudaError_t launch_vector(const SegCopy& c, cudaStream_t s) {
     kernel<<<static_cast<int>(blocks), 256, 0, s>>>(c, per_warp);
     return cudaGetLastError();
   };
-  if (align % 16 == 0) return launch(segment_copy_kernel<uint4>);
-  if (align % 8 == 0) return launch(segment_copy_kernel<uint2>);
-  if (align % 4 == 0) return launch(segment_copy_kernel<uint32_t>);
-  return launch(segment_copy_kernel<uint8_t>);
+  if (align % 16 == 0)
+    return launch_parts(segment_copy_parts_kernel<uint4>, 16) ? cudaGetLastError() : launch(segment_copy_kernel<uint4>);
+  if (align % 8 == 0)
+    return launch_parts(segment_copy_parts_kernel<uint2>, 8) ? cudaGetLastError() : launch(segment_copy_kernel<uint2>);
+  if (align % 4 == 0)
+    return launch_parts(segment_copy_parts_kernel<uint32_t>, 4) ? cudaGetLastError()
+                                                                : launch(segment_copy_kernel<uint32_t>);
+  return launch_parts(segment_copy_parts_kernel<uint8_t>, 1) ? cudaGetLastError() : launch(segment_copy_kernel<uint8_t>);
 }
 
 // The bulk-eligible, non-empty copies go in batches of up to kMaxBulkBatch;
