@@ -6,9 +6,11 @@
 //   p_ij = exp(scale q_i.k_j - lse_i),  ds_ij = p_ij (dout_i.v_j - delta_i),
 //   dv_j = sum_i p_ij dout_i,  dk_j = scale sum_i ds_ij q_i,  dq_i = scale sum_j ds_ij k_j.
 //
-// Two kernels, neither with atomics, each walking its lap in 64-row
-// sub-steps whose S / dP pair alternates between two TMEM slots, so that the
-// row pass of one sub-step runs while the tensor cores work on the other's:
+// Two kinds of CTA, in one launch (attn_bwd_tc_kernel: the dk/dv CTAs first,
+// then the dq CTAs, which fill the SMs the last wave of dk/dv CTAs leaves
+// idle), neither with atomics, each walking its lap in 64-row sub-steps whose
+// S / dP pair alternates between two TMEM slots, so that the row pass of one
+// sub-step runs while the tensor cores work on the other's:
 //
 // dk / dv: one CTA owns a tile of 128 keys of one (batch entry, head) and
 // walks every 64-row query sub-tile of the lap, rank by rank in the order its
